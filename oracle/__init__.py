@@ -1,0 +1,113 @@
+"""CPU oracle for exact attention (fp64).  TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import this package.  The product path (the CUDA library and its Python binding) never
+imports it, and this package imports nothing from the product path.
+
+``attn_fwd`` / ``attn_bwd`` wrap the plain-C fp64 implementation in ``attn_oracle.c``
+(materialised S and P, chain-rule gradients); ``tiled`` holds a step-by-step fp32
+emulation of the tiled online softmax with the conditional rescale.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``liboracle.so`` (gcc, OpenMP, fp64)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i, p, dbl = ctypes.c_int, ctypes.c_void_p, ctypes.c_double
+            lib.oracle_attn_fwd.argtypes = [p, p, p, i, i, i, i, i, i, dbl, i, p, p, p]
+            lib.oracle_attn_fwd.restype = i
+            lib.oracle_attn_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, dbl, i, p, p, p, p]
+            lib.oracle_attn_bwd.restype = i
+            _lib = lib
+    return _lib
+
+
+def _bits(t) -> np.ndarray:
+    """bf16 torch tensor (or uint16 numpy array of bf16 bit patterns) -> contiguous uint16."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint16
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype == torch.bfloat16, t.dtype
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, heads=None):
+    """fp64 forward.  ``q [B,Hq,N,d]``, ``k``/``v [B,Hkv,N,d]`` in bf16.
+
+    ``heads``: list of (b, hq) to compute (default: all).  Returns (O, LSE) with shapes
+    ``[len(heads), N, d]`` and ``[len(heads), N]`` (or ``[B,Hq,N,d]``/``[B,Hq,N]`` when
+    ``heads`` is None)."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, Hq, N, d = qb.shape
+    Hkv = kb.shape[1]
+    if heads is None:
+        sel = np.arange(B * Hq, dtype=np.int32)
+    else:
+        sel = np.asarray([b * Hq + h for b, h in heads], dtype=np.int32)
+    O = np.zeros((len(sel), N, d), dtype=np.float64)
+    L = np.zeros((len(sel), N), dtype=np.float64)
+    rc = _load().oracle_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, N, d, int(bool(causal)),
+                                 float(scale), len(sel), _ptr(sel), _ptr(O), _ptr(L))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
+    if heads is None:
+        return O.reshape(B, Hq, N, d), L.reshape(B, Hq, N)
+    return O, L
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float, kv_heads=None):
+    """fp64 backward by the chain rule.
+
+    ``kv_heads``: list of (b, hkv) to compute (default: all).  Returns (dQ, dK, dV) with
+    shapes ``[S, g, N, d]``, ``[S, N, d]``, ``[S, N, d]`` for S selected key/value heads
+    (or ``[B,Hq,N,d]``, ``[B,Hkv,N,d]``, ``[B,Hkv,N,d]`` when ``kv_heads`` is None)."""
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(do)
+    B, Hq, N, d = qb.shape
+    Hkv = kb.shape[1]
+    g = Hq // Hkv
+    if kv_heads is None:
+        sel = np.arange(B * Hkv, dtype=np.int32)
+    else:
+        sel = np.asarray([b * Hkv + h for b, h in kv_heads], dtype=np.int32)
+    dQ = np.zeros((len(sel), g, N, d), dtype=np.float64)
+    dK = np.zeros((len(sel), N, d), dtype=np.float64)
+    dV = np.zeros((len(sel), N, d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), B, Hq, Hkv, N, d,
+                                 int(bool(causal)), float(scale), len(sel), _ptr(sel),
+                                 _ptr(dQ), _ptr(dK), _ptr(dV))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd failed ({rc})")
+    if kv_heads is None:
+        return dQ.reshape(B, Hq, N, d), dK.reshape(B, Hkv, N, d), dV.reshape(B, Hkv, N, d)
+    return dQ, dK, dV
