@@ -1,0 +1,178 @@
+"""Python binding for libattn.so: fused exact attention on GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the compiled
+library is missing this module raises at import time; there is no fallback.
+
+Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_bwd``,
+``attn_bwd_workspace_size``, ``attn_last_error`` and the test/tuning knobs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() (or python -m "
+                      "attention_attn_fwd_09_gb300._build) first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_p, _i, _f, _ll, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+_lib.attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]
+_lib.attn_fwd.restype = _i
+_lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
+_lib.attn_bwd.restype = _i
+_lib.attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+_lib.attn_bwd_workspace_size.restype = _sz
+_lib.attn_last_error.argtypes = []
+_lib.attn_last_error.restype = ctypes.c_char_p
+_lib.attn_version.argtypes = []
+_lib.attn_version.restype = ctypes.c_char_p
+_lib.attn_set_debug_knobs.argtypes = [_f, _i, _ll, _i]
+_lib.attn_set_debug_knobs.restype = _i
+_lib.attn_get_debug_knobs.argtypes = [ctypes.POINTER(_f), ctypes.POINTER(_i), ctypes.POINTER(_ll), ctypes.POINTER(_i)]
+_lib.attn_get_debug_knobs.restype = _i
+_lib.attn_device_status.argtypes = [_i]
+_lib.attn_device_status.restype = _i
+_lib.attn_rescale_counter.argtypes = [_i, ctypes.POINTER(ctypes.c_ulonglong)]
+_lib.attn_rescale_counter.restype = _i
+_lib.attn_set_test_hooks.argtypes = [_i]
+_lib.attn_set_test_hooks.restype = _i
+_lib.attn_exp2_sw.argtypes = [_p, _p, _ll, _i, _p]
+_lib.attn_exp2_sw.restype = _i
+
+STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_MISALIGNED",
+          -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA", -6: "ATTN_ERR_TIMEOUT"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def attn_last_error() -> str:
+    return (_lib.attn_last_error() or b"").decode()
+
+
+def attn_version() -> str:
+    return _lib.attn_version().decode()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise AttnError(rc, attn_last_error())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dev_bf16(name, t, shape):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected a contiguous CUDA bf16 tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v).  q [B,Hq,N,d], k/v [B,Hkv,N,d] CUDA bf16.
+
+    ``o`` ([B,Hq,N,d] bf16) and ``lse`` ([B,Hq,N] fp32) may be given to reuse buffers."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    _dev_bf16("q", q, (B, Hq, N, d))
+    _dev_bf16("k", k, (B, Hkv, N, d))
+    _dev_bf16("v", v, (B, Hkv, N, d))
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _dev_bf16("o", o, (B, Hq, N, d))
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, N):
+        raise ValueError("lse: expected a contiguous fp32 tensor [B,Hq,N]")
+    _check(_lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)),
+                         float(scale), _stream(stream)))
+    return o, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, d: int, deterministic: bool = False) -> int:
+    n = _lib.attn_bwd_workspace_size(B, Hq, Hkv, N, d, int(bool(deterministic)))
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError(-1, attn_last_error())
+    return int(n)
+
+
+def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, deterministic: bool = False,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of attention given the forward's o, lse and the upstream gradient do."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    for name, t, shp in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
+                         ("o", o, (B, Hq, N, d)), ("do", do, (B, Hq, N, d))):
+        _dev_bf16(name, t, shp)
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d, deterministic)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=q.device)
+    _check(_lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                         B, Hq, Hkv, N, d, int(bool(causal)), float(scale), int(bool(deterministic)),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+def attn_set_debug_knobs(tau: float = 8.0, poly_per_16: int = 0, wait_limit_ns: int = 2_000_000_000,
+                         sync_check: bool = False):
+    _check(_lib.attn_set_debug_knobs(float(tau), int(poly_per_16), int(wait_limit_ns), int(bool(sync_check))))
+
+
+def attn_get_debug_knobs():
+    tau, poly, wl, sc = _f(), _i(), _ll(), _i()
+    _check(_lib.attn_get_debug_knobs(ctypes.byref(tau), ctypes.byref(poly), ctypes.byref(wl), ctypes.byref(sc)))
+    return {"tau": tau.value, "poly_per_16": poly.value, "wait_limit_ns": wl.value, "sync_check": bool(sc.value)}
+
+
+def attn_set_test_hooks(skip_first_kv_load: bool = False):
+    _check(_lib.attn_set_test_hooks(int(bool(skip_first_kv_load))))
+
+
+def attn_device_status(clear: bool = True) -> int:
+    """Synchronise and return the raw status (0 = fine, ATTN_ERR_TIMEOUT = a kernel gave up)."""
+    return int(_lib.attn_device_status(int(bool(clear))))
+
+
+def attn_rescale_counter(enable: bool) -> int:
+    v = ctypes.c_ulonglong(0)
+    _check(_lib.attn_rescale_counter(int(bool(enable)), ctypes.byref(v)))
+    return int(v.value)
+
+
+def attn_exp2_sw(x, variant: int = 0, stream=None):
+    """y = 2^x on the GPU: variant 0 = polynomial as used in the forward, 1 = polynomial
+    with correct subnormals, 2 = MUFU ex2.approx."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x: contiguous CUDA fp32 tensor expected")
+    y = torch.empty_like(x)
+    _check(_lib.attn_exp2_sw(_ptr(x), _ptr(y), x.numel(), int(variant), _stream(stream)))
+    return y
+
+
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_last_error", "attn_version",
+           "attn_set_debug_knobs", "attn_get_debug_knobs", "attn_device_status", "attn_rescale_counter",
+           "attn_exp2_sw", "attn_set_test_hooks", "AttnError", "LIB_PATH"]

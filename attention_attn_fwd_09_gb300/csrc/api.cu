@@ -1,0 +1,306 @@
+// C-ABI entry points (declared in include/attn.h): argument checks, TMA tensor maps,
+// kernel selection and launch.  No allocation on any call path; every launch goes on
+// the caller's stream.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+namespace attn {
+
+// Status word written by kernels that give up on a bounded wait, and the optional
+// rescale counter.  One copy per device; the host reaches them through their device
+// addresses (cudaGetSymbolAddress, cached per device).
+__device__ int g_dev_status;
+__device__ unsigned long long g_rescale_count;
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof t_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(ATTN_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::atomic<float> g_tau{8.0f};
+std::atomic<int> g_poly{0};
+std::atomic<long long> g_wait_ns{2000000000LL};
+std::atomic<int> g_sync_check{0};
+std::atomic<int> g_count_rescales{0};
+std::atomic<int> g_test_skip_kv{0};
+
+struct DevSyms {
+  int* status = nullptr;
+  unsigned long long* rescale = nullptr;
+  int sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+constexpr int kMaxDev = 64;
+DevSyms g_syms[kMaxDev];
+std::once_flag g_syms_once[kMaxDev];
+
+const DevSyms* dev_syms(int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    static DevSyms bad;
+    bad.err = e;
+    return &bad;
+  }
+  if (dev_out) *dev_out = dev;
+  DevSyms& s = g_syms[dev % kMaxDev];
+  std::call_once(g_syms_once[dev % kMaxDev], [&] {
+    void* p = nullptr;
+    s.err = cudaGetSymbolAddress(&p, g_dev_status);
+    s.status = static_cast<int*>(p);
+    if (s.err == cudaSuccess) {
+      s.err = cudaGetSymbolAddress(&p, g_rescale_count);
+      s.rescale = static_cast<unsigned long long*>(p);
+    }
+    if (s.err == cudaSuccess) s.err = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  return &s;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time
+// dependency on libcuda).
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+EncodeFn get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess) g_encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  return g_encode;
+}
+
+// [BH, rows, d] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
+int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, const char* name) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(g_encode_err));
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "tensor map for %s: CUresult %d", name, (int)r);
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
+  if (B < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "B=%d and N=%d must be >= 0", B, N);
+  if (Hq <= 0 || Hkv <= 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d and Hkv=%d must be >= 1", Hq, Hkv);
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if ((long long)B * Hq > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "B*Hq too large");
+  return ATTN_OK;
+}
+
+int post_launch(const DevSyms* s, cudaStream_t st) {
+  if (!g_sync_check.load()) return ATTN_OK;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, s->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (v != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a bounded wait (device status %d)", v);
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_last_error(void) { return t_err; }
+
+const char* attn_version(void) { return "attn-gb300 0.1 (sm_103a)"; }
+
+int attn_set_debug_knobs(float tau, int poly_per_16, long long wait_limit_ns, int sync_check) {
+  if (!(tau >= 0.0f) || !std::isfinite(tau)) return fail(ATTN_ERR_INVALID_ARG, "tau must be finite and >= 0");
+  if (poly_per_16 != 0 && poly_per_16 != 4 && poly_per_16 != 16)
+    return fail(ATTN_ERR_UNSUPPORTED, "poly_per_16=%d (supported: 0, 4, 16)", poly_per_16);
+  if (wait_limit_ns <= 0) return fail(ATTN_ERR_INVALID_ARG, "wait limit must be > 0");
+  g_tau.store(tau);
+  g_poly.store(poly_per_16);
+  g_wait_ns.store(wait_limit_ns);
+  g_sync_check.store(sync_check ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_set_test_hooks(int skip_first_kv_load) {
+  g_test_skip_kv.store(skip_first_kv_load ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_get_debug_knobs(float* tau, int* poly_per_16, long long* wait_limit_ns, int* sync_check) {
+  if (tau) *tau = g_tau.load();
+  if (poly_per_16) *poly_per_16 = g_poly.load();
+  if (wait_limit_ns) *wait_limit_ns = g_wait_ns.load();
+  if (sync_check) *sync_check = g_sync_check.load();
+  return ATTN_OK;
+}
+
+int attn_device_status(int clear) {
+  const DevSyms* s = dev_syms(nullptr);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device symbols");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, s->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (clear) {
+    const int z = 0;
+    e = cudaMemcpy(s->status, &z, sizeof z, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  }
+  if (v != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a bounded wait (device status %d)", v);
+  return ATTN_OK;
+}
+
+int attn_rescale_counter(int enable, unsigned long long* value_out) {
+  const DevSyms* s = dev_syms(nullptr);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device symbols");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  unsigned long long v = 0;
+  e = cudaMemcpy(&v, s->rescale, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "counter read");
+  if (value_out) *value_out = v;
+  const unsigned long long z = 0;
+  e = cudaMemcpy(s->rescale, &z, sizeof z, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "counter clear");
+  g_count_rescales.store(enable ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, void* stream) {
+  int rc = check_shape(B, Hq, Hkv, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_MISALIGNED, "q, k, v, o and lse must be 16-byte aligned");
+  int dev = 0;
+  const DevSyms* s = dev_syms(&dev);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+
+  FwdMaps maps;
+  if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.k, k, d, N, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.v, v, d, N, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.o, o, d, N, (long long)B * Hq, "o")) != ATTN_OK) return rc;
+
+  FwdParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.pair_heads = (p.g >= 2 && p.g % 2 == 0) ? 1 : 0;
+  p.n_qblk = (N + 127) / 128;
+  p.n_kvblk = p.n_qblk;
+  p.n_rowslots = p.pair_heads ? p.n_qblk : (p.n_qblk + 1) / 2;
+  p.units_per_row = p.pair_heads ? B * (Hq / 2) : B * Hq;
+  p.c = scale * 1.4426950408889634f;
+  p.tau = g_tau.load();
+  p.lse = lse;
+  p.wait_ns = (unsigned long long)g_wait_ns.load();
+  p.status = s->status;
+  p.rescale_count = g_count_rescales.load() ? s->rescale : nullptr;
+  p.test_skip_first_kv = g_test_skip_kv.load();
+  const long long grid = (long long)p.n_rowslots * p.units_per_row;
+  if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_fwd(maps, p, d, g_poly.load(), (int)grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return post_launch(s, st);
+}
+
+int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* stream) {
+  if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
+  if (n > 0 && (!x || !y)) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (variant < 0 || variant > 2) return fail(ATTN_ERR_INVALID_ARG, "variant must be 0, 1 or 2");
+  cudaError_t e = launch_exp2_test(x, y, n, variant, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "exp2 launch");
+  return ATTN_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int deterministic) {
+  if (check_shape(B, Hq, Hkv, N, d, 1.0f) != ATTN_OK) return (size_t)-1;
+  if (B == 0 || N == 0) return 0;
+  return bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_shape(B, Hq, Hkv, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (B == 0 || N == 0) return ATTN_OK;
+  const size_t need = bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return fail(ATTN_ERR_MISALIGNED, "every tensor and the workspace must be 16-byte aligned");
+  int dev = 0;
+  const DevSyms* s = dev_syms(&dev);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+  BwdMaps maps;
+  if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.k, k, d, N, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.v, v, d, N, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dout, dout, d, N, (long long)B * Hq, "dout")) != ATTN_OK) return rc;
+  BwdParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv; p.D = d;
+  p.causal = causal ? 1 : 0;
+  p.deterministic = deterministic ? 1 : 0;
+  p.scale = scale;
+  p.c = scale * 1.4426950408889634f;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  bwd_workspace_carve(workspace, B, Hq, Hkv, N, d, deterministic, &p);
+  p.wait_ns = (unsigned long long)g_wait_ns.load();
+  p.status = s->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd(maps, p, st);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward not available for these arguments");
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return post_launch(s, st);
+}
+
+}  // extern "C"

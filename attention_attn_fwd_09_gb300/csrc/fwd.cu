@@ -1,0 +1,528 @@
+// Fused exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes: O = softmax(scale * Q K^T [causal]) V and LSE (natural log), with the
+// N x N scores never leaving the SM ("Algorithm analysis" page, section 4: tiling so
+// the N x N matrix is never formed).
+//
+// How (the FlashAttention-4 forward pipeline, "Hotelren FA4 summary" section 3.1 and
+// "FlashAttention-4 explained" figure 3, re-laid out for this GPU):
+//   * one CTA owns two 128-row query tiles ("high/low" tiles, section 3.1 item 1): two
+//     row blocks of one head, or, for grouped heads, the same row block of two query
+//     heads that share one K/V head, so every K/V tile loaded serves both (the MQA K/V
+//     reuse of the reverse-engineering page);
+//   * warp 0 is the TMA producer (Q tiles once, K/V tiles through a ring of slots);
+//   * warp 1 issues tcgen05.mma: S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with P read
+//     from TMEM (S and P share columns, "Hotelren FA4 summary" section 4.2 item 1);
+//   * warpgroups 1 and 2 are the softmax of tile 0 and tile 1: while one does its
+//     exponentials the tensor core works on the other tile (section 3.1 item 2);
+//   * warpgroup 3 is the correction group: it rescales O in TMEM only when a row's
+//     running maximum grew by more than tau (section 3.3, tau = 8 in log2 units), and
+//     does the epilogue: O / l -> bf16 -> shared memory -> TMA store, plus the LSE;
+//   * exponentials: each softmax thread sends a fixed subset of its elements through
+//     the FMA-pipe cubic (exp2poly.cuh) and the rest through MUFU.EX2 (section 3.2,
+//     mixed execution).
+//
+// TMEM (512 columns, fp32): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D).
+// P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+#include <cstdint>
+#include <mutex>
+
+#include "exp2poly.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NCH = D / 64;                          // 64-column (128-byte) chunks
+  static constexpr uint32_t CHUNK = 128 * 128;                // bytes of one 128 x 64 bf16 box
+  static constexpr uint32_t TILE = CHUNK * NCH;               // one 128 x D bf16 tile
+  static constexpr int NS = (D == 128) ? 4 : 8;               // K/V ring slots
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_RING = 2 * TILE;
+  static constexpr uint32_t OFF_CTRL = OFF_RING + NS * TILE;
+  // control block: barriers then per-row buffers
+  static constexpr uint32_t CTRL_BYTES = 256 + 6 * 128 * 4 + 64;
+  static constexpr uint32_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+};
+
+// Barrier indices inside the control block (8 bytes each).
+enum {
+  B_Q = 0,
+  B_SFULL = 1,    // +t
+  B_PFULL = 3,    // +t
+  B_STATS = 5,    // +t
+  B_OREADY = 7,   // +t
+  B_OFULL = 9,    // +t
+  B_DONE = 11,
+  B_FULL = 12,    // +slot (up to 8)
+  B_EMPTY = 20,   // +slot
+  B_EPI = 28,     // +t: the tile's O rows are staged in shared memory
+  B_FIN = 30,     // +t: final row statistics (m, l) written (one phase only)
+  B_COUNT = 32
+};
+
+// A wait whose outcome is the same for all 32 lanes (the lanes then run .sync.aligned
+// tcgen05 instructions together).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
+
+// Which of a row's 128 elements go through the FMA polynomial: POLY of every 16, spread
+// evenly (i = 16/POLY - 1, 2*16/POLY - 1, ...), so both pipes stay busy along the row.
+template <int POLY>
+__device__ __forceinline__ constexpr bool poly_lane(int i) {
+  if constexpr (POLY <= 0) {
+    return false;
+  } else if constexpr (POLY >= 16) {
+    return true;
+  } else {
+    constexpr int stride = 16 / POLY;
+    return (i % stride) == stride - 1;
+  }
+}
+
+struct Tiles {
+  int n[2];       // key blocks per tile (0 = tile absent)
+  int row0[2];    // first query row of each tile
+  int bh[2];      // b * Hq + hq of each tile
+  int bkv;        // b * Hkv + hkv
+};
+
+__device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
+  Tiles T;
+  int hu, rs;
+  if (p.causal) {  // longest rows first
+    rs = p.n_rowslots - 1 - unit / p.units_per_row;
+    hu = unit % p.units_per_row;
+  } else {         // all row slots of a head back to back: K/V stay hot in L2
+    hu = unit / p.n_rowslots;
+    rs = unit % p.n_rowslots;
+  }
+  int b, hq0, hq1, r0, r1;
+  if (p.pair_heads) {
+    const int pairs = p.Hq / 2;
+    b = hu / pairs;
+    hq0 = 2 * (hu % pairs);
+    hq1 = hq0 + 1;
+    r0 = r1 = rs * 128;
+  } else {
+    b = hu / p.Hq;
+    hq0 = hq1 = hu % p.Hq;
+    r0 = 2 * rs * 128;
+    r1 = r0 + 128;
+  }
+  const int rows[2] = {r0, r1};
+  const int hqs[2] = {hq0, hq1};
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    T.row0[t] = rows[t];
+    T.bh[t] = b * p.Hq + hqs[t];
+    if (rows[t] >= p.N) {
+      T.n[t] = 0;
+    } else if (p.causal) {
+      const int last = min(rows[t] + 127, p.N - 1);
+      T.n[t] = last / 128 + 1;
+    } else {
+      T.n[t] = p.n_kvblk;
+    }
+  }
+  T.bkv = b * p.Hkv + hq0 / p.g;
+  return T;
+}
+
+template <int D, int POLY>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint8_t* ctrl = smem + C::OFF_CTRL;
+  const uint32_t bar0 = smem_u32(ctrl);
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * i; };
+  float* alpha_buf = reinterpret_cast<float*>(ctrl + 256);        // [2][128]
+  float* m_fin = alpha_buf + 256;                                 // [2][128]
+  float* l_fin = m_fin + 256;                                     // [2][128]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_fin + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int wg = warp >> 2;
+  const Tiles T = map_unit(p, blockIdx.x);
+  const int nmax = max(T.n[0], T.n[1]);
+  WaitCtl wc{p.wait_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_Q), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(B_SFULL + t), 1);
+      mbar_init(BAR(B_PFULL + t), 128);
+      mbar_init(BAR(B_STATS + t), 128);
+      mbar_init(BAR(B_OREADY + t), 128);
+      mbar_init(BAR(B_OFULL + t), 1);
+    }
+    mbar_init(BAR(B_DONE), 1);
+    mbar_init(BAR(B_EPI + 0), 128);
+    mbar_init(BAR(B_EPI + 1), 128);
+    mbar_init(BAR(B_FIN + 0), 128);
+    mbar_init(BAR(B_FIN + 1), 128);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(BAR(B_FULL + s), 1);
+      mbar_init(BAR(B_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Register split (per thread): warpgroup 0 (producer, MMA) 56, softmax 192 + 192,
+  // correction 72: 56 + 192 + 192 + 72 = 512 = 4 x 128, the launch's 128 x 512 threads.
+  // Each role's code sits inside its own branch so that the raised limit covers it.
+  if (wg == 0) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
+      const uint32_t qbytes = (T.n[0] > 0 ? C::TILE : 0) + (T.n[1] > 0 ? C::TILE : 0);
+      mbar_arrive_expect_tx(BAR(B_Q), qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (T.n[t] == 0) continue;
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sbase + C::OFF_Q + t * C::TILE + c * C::CHUNK, &tm_q, c * 64, T.row0[t], T.bh[t], BAR(B_Q));
+      }
+      // next_idx: one past the last ring index handed to the TMA unit.  skip_idx: a ring
+      // index deliberately never loaded (test hook for the bounded-wait path), or -1.
+      const int skip_idx = p.test_skip_first_kv ? 0 : -1;
+      int next_idx = 0;
+      bool ok = true;
+      for (int j = 0; j < nmax && ok; ++j) {
+        for (int which = 0; which < 2; ++which) {
+          const int idx = 2 * j + which, slot = idx % C::NS, round = idx / C::NS;
+          if (round > 0 && !mbar_wait(BAR(B_EMPTY + slot), (round - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          next_idx = idx + 1;
+          if (idx == skip_idx) continue;
+          mbar_arrive_expect_tx(BAR(B_FULL + slot), C::TILE);
+          const CUtensorMap* tm = which ? &tm_v : &tm_k;
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, T.bkv,
+                        BAR(B_FULL + slot));
+        }
+      }
+      if (!ok) {
+        // Let the copies still in flight land before the CTA's shared memory goes away:
+        // only the last NS ring indices can be outstanding.
+        const unsigned long long t0 = globaltimer_ns();
+        for (int idx = max(0, next_idx - C::NS); idx < next_idx; ++idx) {
+          if (idx == skip_idx) continue;
+          const uint32_t bar = BAR(B_FULL + idx % C::NS), par = (idx / C::NS) & 1;
+          while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 < p.wait_ns) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + D};
+      bool ok = mbar_wait(BAR(B_Q), 0, wc);
+      tc_fence_after();
+      for (int j = 0; j <= nmax && ok; ++j) {
+        const int kidx = 2 * j, kslot = kidx % C::NS;
+        const int vidx = 2 * (j - 1) + 1, vslot = (vidx + C::NS) % C::NS;
+        if (j < nmax && !mbar_wait(BAR(B_FULL + kslot), (kidx / C::NS) & 1, wc)) { ok = false; break; }
+        if (j >= 1 && !mbar_wait(BAR(B_FULL + vslot), (vidx / C::NS) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = sbase + C::OFF_RING + kslot * C::TILE;
+        const uint32_t vbase = sbase + C::OFF_RING + vslot * C::TILE;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= 1 && j <= T.n[t]) {
+            // O_t += P_t(j-1) V_(j-1): needs the softmax's P and the correction's go-ahead.
+            if (!mbar_wait(BAR(B_PFULL + t), (j - 1) & 1, wc) || !mbar_wait(BAR(B_OREADY + t), (j - 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024);
+              mma_ts(tO[t], tS[t] + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(BAR(B_OFULL + t));
+          }
+          if (j < T.n[t]) {
+            // S_t = Q_t K_j^T
+            const uint32_t qbase = sbase + C::OFF_Q + t * C::TILE;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+              mma_ss(tS[t], sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(BAR(B_SFULL + t));
+          }
+        }
+        if (!ok) break;
+        if (j < nmax) mma_commit(BAR(B_EMPTY + kslot));
+        if (j >= 1) mma_commit(BAR(B_EMPTY + vslot));
+      }
+      // Drain: every MMA issued above completes before TMEM is released.
+      mma_commit(BAR(B_DONE));
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(BAR(B_DONE), 0) && globaltimer_ns() - t0 < p.wait_ns) {
+      }
+    }
+  }
+  } else if (wg == 1 || wg == 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+    // ------------------------------------------------------------------ softmax
+    const int t = wg - 1;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + uint32_t(t * 128);
+    const int grow = T.row0[t] + row;
+    const float c = p.c;
+    float m = -INFINITY, l = 0.f;
+    const int n_t = T.n[t];
+    for (int j = 0; j < n_t; ++j) {
+      if (!warp_wait(BAR(B_SFULL + t), j & 1, wc)) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tmem_ld32(tS + q * 32, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(r[i]);
+        }
+      }
+      const int kb = j * 128;
+      const bool need_mask = (kb + 127 >= p.N) || (p.causal && kb + 127 > T.row0[t]);
+      if (need_mask) {
+        const int lim = (p.causal ? min(grow, p.N - 1) : p.N - 1) - kb;  // last visible column
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx[a] = s[a];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_cand = fmaxf(m, rmax * c);
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_cand;
+      } else if (m_cand - m > p.tau) {
+        alpha = ex2_mufu(m - m_cand);
+        m = m_cand;
+      }
+      alpha_buf[t * 128 + row] = alpha;
+      mbar_arrive(BAR(B_STATS + t));
+      const float neg_m = -m;
+      float acc[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const float x = fmaf(s[i], c, neg_m);
+        const float e = poly_lane<POLY>(i) ? exp2_poly(x) : ex2_mufu(x);
+        s[i] = e;
+        acc[i & 7] += e;
+      }
+      l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]);
+          tmem_st32(tS + h * 32, pk);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(B_PFULL + t));
+    }
+    // A barrier of its own: arriving on B_STATS again here could complete that
+    // barrier's last two phases before the correction group waits on the first.
+    m_fin[t * 128 + row] = m;
+    l_fin[t * 128 + row] = l;
+    mbar_arrive(BAR(B_FIN + t));
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+    // ------------------------------------------------------------------ correction + epilogue
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int j = 0; j < nmax && ok; ++j) {
+      for (int t = 0; t < 2; ++t) {
+        if (j >= T.n[t]) continue;
+        if (!warp_wait(BAR(B_STATS + t), j & 1, wc)) { ok = false; break; }
+        const float alpha = alpha_buf[t * 128 + row];
+        const bool any = __any_sync(0xffffffffu, alpha != 1.f);
+        if (p.rescale_count != nullptr && j > 0) {
+          const unsigned bal = __ballot_sync(0xffffffffu, alpha != 1.f);
+          if (lane == 0 && bal) atomicAdd(p.rescale_count, (unsigned long long)__popc(bal));
+        }
+        if (j > 0 && any) {
+          if (!warp_wait(BAR(B_OFULL + t), (j - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
+          uint32_t r[32];
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            tmem_ld32(tO + q * 32, r);
+            tmem_wait_ld();
+            reg_fence(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + q * 32, r);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_OREADY + t));
+      }
+    }
+    // Epilogue per tile: O / l -> bf16 -> swizzled shared memory (the tile's Q buffer,
+    // free once its last MMA completed) -> TMA store; LSE straight to global memory.
+    for (int t = 0; t < 2 && ok; ++t) {
+      const int n_t = T.n[t];
+      if (n_t == 0) continue;
+      if (!warp_wait(BAR(B_FIN + t), 0, wc)) { ok = false; break; }
+      if (!warp_wait(BAR(B_OFULL + t), (n_t - 1) & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const float mrow = m_fin[t * 128 + row], lrow = l_fin[t * 128 + row];
+      const float inv = 1.f / lrow;
+      const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
+      uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
+      uint32_t r[32];
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {
+        tmem_ld32(tO + q * 32, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        const int box = (q * 32) / 64, j0 = ((q * 32) % 64) / 8;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t off = box * C::CHUNK + row * 128 + (((j0 + u) ^ (row & 7)) * 16);
+          *reinterpret_cast<uint4*>(stage + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      const int grow = T.row0[t] + row;
+      if (grow < p.N) p.lse[(size_t)T.bh[t] * p.N + grow] = (mrow + __log2f(lrow)) * kLn2;
+      fence_proxy_async_smem();
+      mbar_arrive(BAR(B_EPI + t));
+      if (warp == 12 && lane == 0 && mbar_wait(BAR(B_EPI + t), 0, wc)) {
+        for (int c = 0; c < C::NCH; ++c)
+          tma_store_3d(&tm_o, sbase + C::OFF_Q + t * C::TILE + c * C::CHUNK, c * 64, T.row0[t], T.bh[t]);
+        tma_store_commit();
+      }
+    }
+    if (warp == 12 && lane == 0) tma_store_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int POLY>
+cudaError_t launch_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
+  auto kern = attn_fwd_kernel<D, POLY>;
+  constexpr uint32_t smem = FwdCfg<D>::SMEM;
+  static std::once_flag flags[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static cudaError_t attr_err[64];
+  std::call_once(flags[dev & 63], [&] {
+    attr_err[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+  kern<<<grid, kThreads, smem, s>>>(m.q, m.k, m.v, m.o, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int D) { return D == 64 ? FwdCfg<64>::SMEM : FwdCfg<128>::SMEM; }
+
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly, int grid, cudaStream_t s) {
+  if (D == 64) {
+    if (poly == 0) return launch_t<64, 0>(maps, p, grid, s);
+    if (poly == 4) return launch_t<64, 4>(maps, p, grid, s);
+    if (poly == 16) return launch_t<64, 16>(maps, p, grid, s);
+  } else if (D == 128) {
+    if (poly == 0) return launch_t<128, 0>(maps, p, grid, s);
+    if (poly == 4) return launch_t<128, 4>(maps, p, grid, s);
+    if (poly == 16) return launch_t<128, 16>(maps, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------------------------
+// Software exp2 test kernel (grid-stride, plain loads/stores).
+// ------------------------------------------------------------------------------------
+__global__ void exp2_test_kernel(const float* __restrict__ x, float* __restrict__ y, long long n, int variant) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    y[i] = variant == 0 ? exp2_poly(v) : (variant == 1 ? exp2_poly_full_range(v) : ex2_mufu(v));
+  }
+}
+
+cudaError_t launch_exp2_test(const float* x, float* y, long long n, int variant, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long blocks = (n + 255) / 256;
+  const int grid = (int)(blocks < (long long)sms * 8 ? blocks : (long long)sms * 8);
+  exp2_test_kernel<<<grid, 256, 0, s>>>(x, y, n, variant);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,64 @@
+// Launch interfaces shared between the host entry points (api.cu) and the kernel
+// translation units.  Host-only types; no torch.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct FwdParams {
+  int B, Hq, Hkv, N, g;
+  int causal;
+  int pair_heads;          // 1: a CTA's two tiles are query heads 2p, 2p+1 of one KV group
+  int n_qblk, n_kvblk;     // ceil(N / 128)
+  int units_per_row;       // CTAs per query-row slot (see fwd.cu unit mapping)
+  int n_rowslots;          // query-row slots per head (pair) sequence
+  float c;                 // scale * log2(e)
+  float tau;               // conditional-rescale threshold, log2 units
+  float* lse;              // [B, Hq, N] fp32, natural log
+  unsigned long long wait_ns;
+  int* status;
+  unsigned long long* rescale_count;  // optional counter (nullptr = off)
+  int test_skip_first_kv;             // test hook: never load ring index 0 (exercises timeouts)
+};
+
+struct FwdMaps {
+  CUtensorMap q, k, v, o;
+};
+
+// Forward: D in {64, 128}; poly_per_16 in {0, 4, 16} elements of every 16 computed by
+// the FMA polynomial instead of MUFU.EX2.
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly_per_16, int grid,
+                       cudaStream_t stream);
+size_t fwd_smem_bytes(int D);
+
+// Software exp2 accuracy / throughput test entry: variant 0 = production polynomial,
+// 1 = full-range polynomial, 2 = MUFU ex2.approx.
+cudaError_t launch_exp2_test(const float* x, float* y, long long n, int variant, cudaStream_t s);
+
+// Backward.
+struct BwdParams {
+  int B, Hq, Hkv, N, g, D;
+  int causal, deterministic;
+  float scale, c;            // softmax scale; scale * log2(e)
+  const void *q, *k, *v, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  float* dq_acc;             // [B, Hq, N, D] fp32 workspace
+  float* delta;              // [B, Hq, N] fp32 workspace (rowsum(dO o O))
+  float* lse2;               // [B, Hq, N] fp32 workspace (LSE * log2 e)
+  int* sem;                  // deterministic-order counters
+  unsigned long long wait_ns;
+  int* status;
+};
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic);
+// Points p->dq_acc, delta, lse2, sem into the caller's workspace.
+void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int deterministic, BwdParams* p);
+
+}  // namespace attn

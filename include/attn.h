@@ -1,0 +1,147 @@
+/*
+ * attn.h -- C ABI of libattn.so: fused exact scaled-dot-product attention on GB300
+ * (sm_103a), forward and backward.
+ *
+ * The operation ("Algorithm analysis" page, section 4; "FlashAttention-4 explained"
+ * page, section 01: attention is two matrix products around a softmax):
+ *
+ *     S = scale * Q K^T          (causal: S_ij = -inf for key j > query i)
+ *     P = softmax(S) row-wise
+ *     O = P V,   LSE_i = ln sum_j exp(S_ij)
+ *
+ * computed tile by tile so that S and P never reach device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are device pointers to contiguous row-major bf16 (__nv_bfloat16 bit
+ *    patterns) unless stated otherwise.  Shapes: Q, O, dO, dQ are [B, Hq, N, d];
+ *    K, V, dK, dV are [B, Hkv, N, d].  LSE is fp32 [B, Hq, N].
+ *  - Grouped heads (GQA/MQA): Hq must be a multiple of Hkv; query head h reads
+ *    key/value head h / (Hq / Hkv).
+ *  - d must be 64 or 128.  N >= 0, B >= 0 (either being 0 is a no-op returning 0).
+ *    Any N >= 1 is supported (a ragged last tile is masked).
+ *  - Every tensor pointer must be 16-byte aligned (TMA requirement).
+ *  - scale > 0 (the usual choice is 1/sqrt(d)).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous:
+ *    they enqueue kernels and return.  The caller owns every buffer and the stream; the
+ *    library allocates no device memory on any call.
+ *  - Return value: ATTN_OK (0) or a negative attn_status.  On error nothing was
+ *    launched and attn_last_error() holds a message (thread-local).
+ *  - Kernels never trap.  Every wait inside a kernel is bounded; a kernel that gives
+ *    up sets a device status word and returns, leaving its outputs undefined.  Read
+ *    (and clear) that word with attn_device_status().
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* bad shape, null pointer, bad scale */
+  ATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. d not in {64,128}) */
+  ATTN_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = -4,   /* backward workspace missing or too small */
+  ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed (message has the name) */
+  ATTN_ERR_TIMEOUT = -6      /* a kernel gave up on a bounded wait */
+} attn_status;
+
+/*
+ * Forward pass.  FlashAttention-4 forward pipeline: "Hotelren FA4 summary" page,
+ * section 3 (two query tiles per CTA, softmax and correction warpgroups, conditional
+ * rescale with tau = 8 in log2 units, exponentials split between MUFU and an FMA
+ * polynomial); "Algorithm analysis" page, section 4 (tiled online softmax).
+ *
+ *   q   [B,Hq,N,d] bf16, in      k, v [B,Hkv,N,d] bf16, in
+ *   o   [B,Hq,N,d] bf16, out     lse  [B,Hq,N] fp32, out: ln sum_j exp(S_ij)
+ *   causal: 0 or 1 (key j visible to query i only if j <= i)
+ *   scale:  softmax scale applied to Q K^T
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ accumulator
+ * [B,Hq,N,d], rowsum(dO o O) and LSE*log2(e) [B,Hq,N], ordering counters).  0 when
+ * there is nothing to do.  Returns (size_t)-1 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int deterministic);
+
+/*
+ * Backward pass: dQ, dK, dV of L given dO = dL/dO.  Recomputes P from Q, K and the
+ * forward's LSE (reverse-engineering page: backward by recomputation).  Stages follow
+ * "Hotelren FA4 summary" page, section 4.2: S = K Q^T, dP = dO V^T, dV = P^T dO,
+ * dS = P o (dP - rowsum(dO o O)), dQ += dS K (fp32 accumulation), dK = dS^T Q.
+ *
+ *   q, k, v, o, lse, dout: the forward's inputs and outputs (o and lse as attn_fwd
+ *       wrote them), dout [B,Hq,N,d] bf16.
+ *   dq [B,Hq,N,d], dk, dv [B,Hkv,N,d] bf16, out (overwritten, not accumulated into).
+ *   deterministic: 1 = dQ contributions are added in a fixed order, so repeated calls
+ *       give bit-identical outputs ("FlashAttention-4 explained" page, section 06);
+ *       0 = unordered fp32 atomics.
+ *   workspace: device memory of at least attn_bwd_workspace_size(...) bytes, 16-byte
+ *       aligned, owned by the caller; its contents on entry do not matter.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* attn_last_error(void);
+
+/* Library version string. */
+const char* attn_version(void);
+
+/*
+ * Tuning and test knobs (process-wide; take effect on the next call):
+ *   tau:           conditional-rescale threshold in log2 units (default 8; 0 = rescale
+ *                  whenever a row maximum grows).  "Hotelren FA4 summary" section 3.3.
+ *   poly_per_16:   exponentials computed by the FMA polynomial, per 16 (0, 4 or 16;
+ *                  default 0).  "Hotelren FA4 summary" section 3.2.
+ *   wait_limit_ns: bound on any single wait inside a kernel (default 2 s).
+ *   sync_check:    1 = each call synchronises its stream and checks the device status
+ *                  word (debugging only).
+ */
+int attn_set_debug_knobs(float tau, int poly_per_16, long long wait_limit_ns, int sync_check);
+int attn_get_debug_knobs(float* tau, int* poly_per_16, long long* wait_limit_ns, int* sync_check);
+
+/*
+ * Test hook (off by default): skip_first_kv_load = 1 makes the forward's load warp never
+ * issue the first K tile of each CTA, so the consumer's bounded wait runs out, the CTA
+ * gives up cleanly and the device status word reads ATTN_ERR_TIMEOUT.  Used to test the
+ * timeout path without faulting anything.  No counterpart on the pages.
+ */
+int attn_set_test_hooks(int skip_first_kv_load);
+
+/*
+ * Synchronises the current device and reads the device status word: ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if some kernel gave up on a wait since the last clear.  clear = 1
+ * resets the word.
+ */
+int attn_device_status(int clear);
+
+/*
+ * Rescale statistics: synchronises, returns in *value_out the number of (row, key tile)
+ * steps after the first tile in which the forward rescaled O (counted only while
+ * enabled), resets the count, and enables (1) or disables (0) counting.
+ */
+int attn_rescale_counter(int enable, unsigned long long* value_out);
+
+/*
+ * Software exp2 test entry: y[i] = 2^x[i] for i < n (device fp32 arrays).
+ *   variant 0: the FMA-pipe polynomial exactly as the forward uses it;
+ *   variant 1: the same polynomial with a correctly rounded subnormal range;
+ *   variant 2: the hardware MUFU ex2.approx.ftz.
+ * "FlashAttention-4 explained" page, section 04: e^x ~ 2^n (p0 + p1 f + p2 f^2 + p3 f^3).
+ */
+int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,96 @@
+"""The C ABI library loads, exports every declared entry point, and rejects bad
+arguments with the documented status codes before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
+    L = ctypes.CDLL(path)
+    p, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+    L.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, p]
+    L.attn_fwd.restype = i
+    L.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p, sz, p]
+    L.attn_bwd.restype = i
+    L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.attn_bwd_workspace_size.restype = sz
+    L.attn_last_error.restype = ctypes.c_char_p
+    L.attn_set_debug_knobs.argtypes = [f, i, ll, i]
+    L.attn_set_debug_knobs.restype = i
+    L.attn_exp2_sw.argtypes = [p, p, ll, i, p]
+    L.attn_exp2_sw.restype = i
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+FAKE = ctypes.c_void_p(0x10000)       # aligned, never dereferenced on the error paths
+MIS = ctypes.c_void_p(0x10008)
+
+
+def fwd(lib, B=1, Hq=2, Hkv=2, N=128, d=64, causal=0, scale=0.125, ptrs=None):
+    q = k = v = o = lse = FAKE
+    if ptrs:
+        q, k, v, o, lse = ptrs
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert fwd(lib, d=96) == -2
+    assert b"d=96" in lib.attn_last_error()
+    assert fwd(lib, Hq=3, Hkv=2) == -1
+    assert fwd(lib, Hkv=0) == -1
+    assert fwd(lib, N=-1) == -1
+    assert fwd(lib, scale=0.0) == -1
+    assert fwd(lib, scale=float("nan")) == -1
+    assert fwd(lib, ptrs=(FAKE, FAKE, MIS, FAKE, FAKE)) == -3
+    assert fwd(lib, ptrs=(FAKE, None, FAKE, FAKE, FAKE)) == -1
+    # Nothing to do: OK without any device work.
+    assert fwd(lib, B=0) == 0
+    assert fwd(lib, N=0) == 0
+
+
+def test_bwd_workspace_and_errors(lib):
+    assert lib.attn_bwd_workspace_size(0, 2, 2, 128, 64, 0) == 0
+    n = lib.attn_bwd_workspace_size(2, 4, 2, 300, 128, 1)
+    assert n >= 2 * 4 * 300 * 128 * 4      # at least the fp32 dQ accumulator
+    assert n % 16 == 0
+    assert lib.attn_bwd_workspace_size(1, 3, 2, 128, 64, 0) == ctypes.c_size_t(-1).value
+    rc = lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 128, 96, 0, 0.1, 0,
+                      FAKE, 1 << 30, None)
+    assert rc == -2
+    rc = lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 128, 64, 0, 0.1, 0,
+                      FAKE, 16, None)
+    assert rc == -4                          # workspace too small
+
+
+def test_knobs_validate(lib):
+    assert lib.attn_set_debug_knobs(-1.0, 0, 1000, 0) == -1
+    assert lib.attn_set_debug_knobs(8.0, 3, 1000, 0) == -2
+    assert lib.attn_set_debug_knobs(8.0, 0, 0, 0) == -1
+    assert lib.attn_set_debug_knobs(8.0, 0, 2_000_000_000, 0) == 0
+
+
+def test_exp2_entry_validates(lib):
+    assert lib.attn_exp2_sw(None, None, -1, 0, None) == -1
+    assert lib.attn_exp2_sw(FAKE, FAKE, 16, 7, None) == -1
+    assert lib.attn_exp2_sw(None, None, 0, 0, None) == 0
