@@ -285,6 +285,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if ((rc = make_map(&maps.k, k, d, N, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.v, v, d, N, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.dout, dout, d, N, (long long)B * Hq, "dout")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dk, dk, d, N, (long long)B * Hkv, "dk")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dv, dv, d, N, (long long)B * Hkv, "dv")) != ATTN_OK) return rc;
   BwdParams p{};
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv; p.D = d;
   p.causal = causal ? 1 : 0;

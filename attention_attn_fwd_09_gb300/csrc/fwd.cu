@@ -47,7 +47,7 @@ struct FwdCfg {
   static constexpr uint32_t OFF_RING = 2 * TILE;
   static constexpr uint32_t OFF_CTRL = OFF_RING + NS * TILE;
   // control block: barriers then per-row buffers
-  static constexpr uint32_t CTRL_BYTES = 256 + 6 * 128 * 4 + 64;
+  static constexpr uint32_t CTRL_BYTES = 256 + 8 * 128 * 4 + 64;
   static constexpr uint32_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* alpha_buf = reinterpret_cast<float*>(ctrl + 256);        // [2][128]
   float* m_fin = alpha_buf + 256;                                 // [2][128]
   float* l_fin = m_fin + 256;                                     // [2][128]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_fin + 256);
+  float* lq_fin = l_fin + 256;                                    // [2][128]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lq_fin + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -312,23 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + uint32_t(t * 128);
     const int grow = T.row0[t] + row;
     const float c = p.c;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lq = 0.f;
     const int n_t = T.n[t];
     for (int j = 0; j < n_t; ++j) {
       if (!warp_wait(BAR(B_SFULL + t), j & 1, wc)) break;
       tc_fence_after();
-      float s[128];
-      {
-        uint32_t r[32];
+      // The whole 128-column row in one batch of TMEM loads and a single wait.
+      uint32_t u[128];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tmem_ld32(tS + q * 32, r);
-          tmem_wait_ld();
-          reg_fence(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(r[i]);
-        }
-      }
+      for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[q * 32]));
+      tmem_wait_ld();
+      reg_fence(u);
+      float* s = reinterpret_cast<float*>(u);
       const int kb = j * 128;
       const bool need_mask = (kb + 127 >= p.N) || (p.causal && kb + 127 > T.row0[t]);
       if (need_mask) {
@@ -337,13 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx[8];
+      float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = s[a];
-#pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-      const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 4; i < 128; i += 8) {
+        mx[0] = fmax3(mx[0], s[i], s[i + 1]);
+        mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+        mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+        if (i + 7 < 128) mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+        else mx[3] = fmaxf(mx[3], s[i + 6]);
+      }
+      const float rmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       const float m_cand = fmaxf(m, rmax * c);
       float alpha = 1.f;
       if (j == 0) {
@@ -354,27 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       alpha_buf[t * 128 + row] = alpha;
       mbar_arrive(BAR(B_STATS + t));
+      // p = 2^(s*c - m).  Two running sums: l over the fp32 p (for LSE) and lq over the
+      // bf16-rounded p the PV product actually uses (for O / lq, which makes a row whose
+      // weight sits on one key come out exact up to the output rounding).
       const float neg_m = -m;
-      float acc[8];
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accq[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[64];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) acc[a] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float x = fmaf(s[i], c, neg_m);
-        const float e = poly_lane<POLY>(i) ? exp2_poly(x) : ex2_mufu(x);
-        s[i] = e;
-        acc[i & 7] += e;
+      for (int i = 0; i < 128; i += 2) {
+        float x0, x1;
+        ffma2_bc(x0, x1, s[i], s[i + 1], c, neg_m);
+        const float e0 = poly_lane<POLY>(i) ? exp2_poly(x0) : ex2_mufu(x0);
+        const float e1 = poly_lane<POLY>(i + 1) ? exp2_poly(x1) : ex2_mufu(x1);
+        const uint32_t pr = pack_bf16x2(e0, e1);
+        pk[i >> 1] = pr;
+        const int a2 = ((i >> 1) & 1) * 2;
+        fadd2(acc[a2], acc[a2 + 1], acc[a2], acc[a2 + 1], e0, e1);
+        fadd2(accq[a2], accq[a2 + 1], accq[a2], accq[a2 + 1], __uint_as_float(pr << 16),
+              __uint_as_float(pr & 0xffff0000u));
       }
-      l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]);
-          tmem_st32(tS + h * 32, pk);
-        }
-      }
+      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      lq = lq * alpha + ((accq[0] + accq[1]) + (accq[2] + accq[3]));
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(B_PFULL + t));
@@ -383,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier's last two phases before the correction group waits on the first.
     m_fin[t * 128 + row] = m;
     l_fin[t * 128 + row] = l;
+    lq_fin[t * 128 + row] = lq;
     mbar_arrive(BAR(B_FIN + t));
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(BAR(B_OFULL + t), (n_t - 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const float mrow = m_fin[t * 128 + row], lrow = l_fin[t * 128 + row];
-      const float inv = 1.f / lrow;
+      const float inv = 1.f / lq_fin[t * 128 + row];
       const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
       uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
       uint32_t r[32];

@@ -54,7 +54,7 @@ struct BwdParams {
   int* status;
 };
 struct BwdMaps {
-  CUtensorMap q, k, v, dout;
+  CUtensorMap q, k, v, dout, dk, dv;
 };
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic);

@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Attention throughput on GB300: TFLOPS of the fused forward + backward step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (one "step" = one pass of the whole hot path over one batch): the training
+shape B=4, Hq=Hkv=16, N=2048, d=128, bf16, non-causal, inputs i.i.d. N(0,1) drawn from a
+seeded generator; the step runs attn_fwd then attn_bwd.  FLOPs: forward 4*B*Hq*N^2*d,
+backward 2.5x that.  Multi-GPU: one process per GPU, every rank runs its own copy of the
+workload (the path shards over independent (batch, head) units with no exchange), so
+scaling is weak and ``value`` is the total over ranks divided by the slowest rank's time.
+
+Printed: one JSON line on rank 0 (see the fields in ``main``).  ``--impl reference``
+times the fp64 CPU oracle on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (BF16, d=128, 1×GB300) and fraction of 2.25 PF peak"
+UNIT = "TFLOP/s"
+NOMINAL_PEAK_TFLOPS = 2250.0
+WORKLOAD = dict(name="train_fwd_bwd_B4_H16_N2048_d128", seed=2, B=4, Hq=16, Hkv=16, N=2048, d=128, causal=False)
+FWD_SWEEP = (4096, 8192, 16384)          # forward-only lines at d=128, non-causal, B*N = 16384
+L2_FLUSH_BYTES = 512 << 20
+
+
+def fwd_flops(B, Hq, N, d, causal):
+    return 4.0 * B * Hq * N * N * d * (0.5 if causal else 1.0)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the forward-only sequence sweep lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    return args
+
+
+# ------------------------------------------------------------------------------ ranks
+def dist_env():
+    """(rank, world, local_rank) from the torchrun environment (1 process = 1 GPU)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def combine(per_rank_units: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units every rank processed / the slowest rank's time."""
+    return per_rank_units * world / max_seconds if max_seconds > 0 else 0.0
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, or None if the kernel's source
+    changed since the counters were taken (the summary stores the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "attention_attn_fwd_09_gb300", "csrc", rec["source"])
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if sha != rec.get("sha256") or rec.get("workload") != WORKLOAD["name"]:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(seconds_fwd: float = 6.0, seconds_bwd: float = 8.0):
+    """Time the fp64 CPU oracle on whole heads of the workload until each leg has run for
+    about the given time.  Returns (flops, seconds, description)."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
+    import oracle
+    from attn_inputs import make_inputs
+    w = WORKLOAD
+    x = make_inputs(w["seed"], w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], with_grad=True)
+    scale = w["d"] ** -0.5
+    oracle.build()
+    ff = fwd_flops(1, 1, w["N"], w["d"], w["causal"])
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["Hq"])]
+    flops, secs, nf, nb = 0.0, 0.0, 0, 0
+    t0 = time.perf_counter()
+    for bh in heads:
+        oracle.attn_fwd(x["q"], x["k"], x["v"], w["causal"], scale, heads=[bh])
+        nf += 1
+        if time.perf_counter() - t0 >= seconds_fwd:
+            break
+    t1 = time.perf_counter()
+    kv = [(b, h) for b in range(w["B"]) for h in range(w["Hkv"])]
+    for bh in kv:
+        oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], w["causal"], scale, kv_heads=[bh])
+        nb += 1
+        if time.perf_counter() - t1 >= seconds_bwd:
+            break
+    t2 = time.perf_counter()
+    g = w["Hq"] // w["Hkv"]
+    flops = nf * ff + nb * g * 2.5 * ff
+    secs = t2 - t0
+    desc = (f"fp64 oracle on {nf} of {len(heads)} query heads (forward) and {nb} of {len(kv)} key/value "
+            f"heads (backward) of the workload, {secs:.1f} s")
+    return flops, secs, desc
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = dist_init(world, "nccl")
+    import attention_attn_fwd_09_gb300 as A
+    from attn_inputs import make_inputs
+
+    w = WORKLOAD
+    B, Hq, Hkv, N, d, causal = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], w["causal"]
+    scale = d ** -0.5
+    x = make_inputs(w["seed"], B, Hq, Hkv, N, d, with_grad=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty((max(A.attn_bwd_workspace_size(B, Hq, Hkv, N, d, False), 16),), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty((L2_FLUSH_BYTES // 4,), dtype=torch.float32, device=dev)
+
+    def fwd():
+        A.attn_fwd(q, k, v, causal=causal, scale=scale, o=o, lse=lse)
+
+    def bwd():
+        A.attn_bwd(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    fwd()
+    try:
+        bwd()
+        has_bwd = True
+    except A.AttnError as e:
+        if e.code != -2:
+            raise
+        has_bwd = False
+    for _ in range(args.warmup):
+        fwd()
+        if has_bwd:
+            bwd()
+    torch.cuda.synchronize()
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+
+    ff = fwd_flops(B, Hq, N, d, causal)
+    step_flops = ff * (3.5 if has_bwd else 1.0)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(K):
+            flush.fill_(float(i))                 # > L2 between timed iterations
+            ev[i][0].record()
+            fwd()
+            ev[i][1].record()
+            if has_bwd:
+                bwd()
+            ev[i][2].record()
+        torch.cuda.synchronize()
+    barrier(dist)
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout during the timed region")
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
+    value = combine(step_flops * K, world, total_s) / 1e12
+
+    # End to end through the public API: pinned host inputs in, results back to the host.
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    q_h, k_h, v_h, do_h = pin(x["q"]), pin(x["k"]), pin(x["v"]), pin(x["do"])
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ((o, dq, dk, dv) if has_bwd else (o,))]
+    h2d = sum(t.numel() * t.element_size() for t in ((q_h, k_h, v_h, do_h) if has_bwd else (q_h, k_h, v_h)))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h) + (lse.numel() * 4)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        ee[i][0].record()
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        if has_bwd:
+            do.copy_(do_h, non_blocking=True)
+        fwd()
+        if has_bwd:
+            bwd()
+        for t_h, t_d in zip(outs_h, (o, dq, dk, dv)):
+            t_h.copy_(t_d, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        ee[i][1].record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e2e_s = max_over_ranks(dist, sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3, dev)
+    e2e_value = combine(step_flops * K, world, e2e_s) / 1e12
+
+    # Forward-only lines at the lengths the forward target is stated for (d=128, non-causal).
+    sweep = {}
+    if not args.no_sweep:
+        for n in FWD_SWEEP:
+            b = 16384 // n
+            g = torch.Generator(device=dev).manual_seed(3)
+            qs = torch.randn((b, 16, n, 128), generator=g, device=dev).to(torch.bfloat16)
+            ks = torch.randn((b, 16, n, 128), generator=g, device=dev).to(torch.bfloat16)
+            vs = torch.randn((b, 16, n, 128), generator=g, device=dev).to(torch.bfloat16)
+            os_, ls = torch.empty_like(qs), torch.empty((b, 16, n), dtype=torch.float32, device=dev)
+            for _ in range(3):
+                A.attn_fwd(qs, ks, vs, causal=False, scale=128 ** -0.5, o=os_, lse=ls)
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
+            for e in evs:
+                flush.fill_(1.0)
+                e[0].record()
+                A.attn_fwd(qs, ks, vs, causal=False, scale=128 ** -0.5, o=os_, lse=ls)
+                e[1].record()
+            torch.cuda.synchronize()
+            ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+            tf = fwd_flops(b, 16, n, 128, False) / ms / 1e9
+            sweep[f"N{n}"] = {"B": b, "ms": round(ms, 4), "tflops": round(tf, 1),
+                              "frac_of_2250": round(tf / NOMINAL_PEAK_TFLOPS, 4)}
+            del qs, ks, vs, os_, ls
+        if A.attn_device_status(True) != 0:
+            raise RuntimeError("a kernel reported a timeout in the sweep")
+
+    peaks, peak_src = measured_peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms) if has_bwd else 0.0
+    dominant = "attn_bwd" if has_bwd and bwd_avg > fwd_avg else "attn_fwd_kernel"
+    if dominant == "attn_fwd_kernel":
+        achieved = ff / fwd_avg / 1e9
+    else:
+        achieved = 2.5 * ff / bwd_avg / 1e9
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "frac_of_2250": round(achieved / NOMINAL_PEAK_TFLOPS, 4),
+                "traffic": recorded_traffic(dominant)}
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16)",
+        "config": {"workload": w["name"], "B": B, "Hq": Hq, "Hkv": Hkv, "seq_len": N, "head_dim": d,
+                   "causal": causal, "passes": "fwd+bwd" if has_bwd else "fwd",
+                   "l2": "512 MiB buffer written between timed iterations",
+                   "parallelism": f"replicas x{world} (independent (batch, head) units)"},
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4) if has_bwd else None,
+        "fwd_tflops": round(ff / fwd_avg / 1e9, 1),
+        "bwd_tflops": round(2.5 * ff / bwd_avg / 1e9, 1) if has_bwd else None,
+        "frac_of_2250": round(value / world / NOMINAL_PEAK_TFLOPS, 4),
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * (1 + (3 if has_bwd else 0)),
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "fwd_sweep_d128_noncausal": sweep,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        flops, secs, desc = oracle_sample()
+        out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),
+                               "kind": "oracle", "sample": desc}
+    if dist is not None:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm, on the host cores, rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
+    import oracle
+    from attn_inputs import make_inputs
+    w = WORKLOAD
+    x = make_inputs(w["seed"], w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], with_grad=True)
+    scale = w["d"] ** -0.5
+    oracle.build()
+    ff = fwd_flops(1, 1, w["N"], w["d"], w["causal"])
+    g = w["Hq"] // w["Hkv"]
+    step_flops = ff + 2.5 * g * ff       # one query head forward + one key/value group backward
+
+    def step(i):
+        b, h = divmod(i % (w["B"] * w["Hkv"]), w["Hkv"])
+        oracle.attn_fwd(x["q"], x["k"], x["v"], w["causal"], scale, heads=[(b, h * g)])
+        oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], w["causal"], scale, kv_heads=[(b, h)])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    secs = time.perf_counter() - t0
+    value = step_flops * args.steps / secs / 1e12
+    desc = (f"per step: fp64 oracle forward of one query head and backward of one key/value head "
+            f"(B=1 slice of {w['name']})")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16 inputs)",
+        "config": {"workload": w["name"], "B": w["B"], "Hq": w["Hq"], "Hkv": w["Hkv"], "seq_len": w["N"],
+                   "head_dim": w["d"], "causal": w["causal"], "passes": "fwd+bwd"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

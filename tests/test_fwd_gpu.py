@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from attn_inputs import WORKLOADS, default_scale, make_inputs, sweep_workload
-from parity import check_fwd
+from parity import check_fwd, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -101,9 +101,13 @@ def test_grouped_outliers_rescale(A, name):
         for s, (b, h) in enumerate(heads):
             check_fwd(o[b, h], lse[b, h], O[s], L[s], f"{name} tau={tau} b{b} h{h}")
     A.attn_set_debug_knobs()
-    # Rescaling on and off give the same result within the forward bounds everywhere.
-    d_all = np.abs(outs[0.0] - outs[8.0]).max()
-    assert d_all <= 2e-2, d_all
+    # Both runs meet the forward bounds against the oracle (above).  Against each other,
+    # over every head: rel. Frobenius <= 1e-2, and elementwise at most one bf16 ulp of the
+    # value (an absolute 2e-2 is below one bf16 ulp once |O| >= 4).
+    a, b8 = outs[0.0].astype(np.float64), outs[8.0].astype(np.float64)
+    assert rel_fro(a, b8) <= 1e-2
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(a), np.abs(b8)) + 1e-30)) - 7)
+    assert (np.abs(a - b8) <= np.maximum(2e-2, ulp)).all(), np.abs(a - b8).max()
     assert counts[8.0] < counts[0.0], counts
     print(f"{name}: rescales tau=0 {counts[0.0]}, tau=8 {counts[8.0]} "
           f"({100.0 * (1 - counts[8.0] / max(counts[0.0], 1)):.1f}% skipped), g={g}")
