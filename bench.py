@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", action="store_true", help="skip the forward-only sequence sweep lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for a profiler: warm-up plus the timed steps only (no e2e, sweep or CPU leg)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -297,6 +299,10 @@ def run_ours(args):
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = combine(step_flops * K, world, total_s) / 1e12
+
+    if args.profile:
+        return {"profile": True, "fwd_ms": round(statistics.mean(fwd_ms), 4),
+                "bwd_ms": round(statistics.mean(bwd_ms), 4) if has_bwd else None} if rank == 0 else None
 
     # End to end through the public API: pinned host inputs in, results back to the host.
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
