@@ -27,6 +27,8 @@ _lib.attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]
 _lib.attn_fwd.restype = _i
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
 _lib.attn_bwd.restype = _i
+_lib.attn_bwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
+_lib.attn_bwd_noalloc.restype = _i
 _lib.attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
 _lib.attn_bwd_workspace_size.restype = _sz
 _lib.attn_last_error.argtypes = []
@@ -137,6 +139,27 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
+def attn_bwd_noalloc(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+                     deterministic: bool = False, dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd without a workspace, for callers that cannot allocate device memory on
+    the call path; the library's own fixed 64 MiB array serves as the workspace (sizes
+    needing more are rejected).  Overlapping calls on different streams race on it."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    for name, t, shp in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
+                         ("o", o, (B, Hq, N, d)), ("do", do, (B, Hq, N, d))):
+        _dev_bf16(name, t, shp)
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(_lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                 int(bool(deterministic)), _stream(stream)))
+    return dq, dk, dv
+
+
 def attn_set_debug_knobs(tau: float = 8.0, poly_per_16: int = 0, wait_limit_ns: int = 2_000_000_000,
                          sync_check: bool = False):
     _check(_lib.attn_set_debug_knobs(float(tau), int(poly_per_16), int(wait_limit_ns), int(bool(sync_check))))
@@ -173,6 +196,6 @@ def attn_exp2_sw(x, variant: int = 0, stream=None):
     return y
 
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_last_error", "attn_version",
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_last_error", "attn_version",
            "attn_set_debug_knobs", "attn_get_debug_knobs", "attn_device_status", "attn_rescale_counter",
            "attn_exp2_sw", "attn_set_test_hooks", "AttnError", "LIB_PATH"]

@@ -136,6 +136,9 @@ int post_launch(const DevSyms* s, cudaStream_t st) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { snprintf(t_err, sizeof t_err, "%s", msg); }
+
 }  // namespace attn
 
 using namespace attn;

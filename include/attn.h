@@ -90,6 +90,25 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory on the call path: code
+ * running inside another runtime's plugin or callback interface (its memory belongs to
+ * that runtime's pool) or in a latency-critical loop where cudaMalloc would
+ * synchronise the device.  No counterpart on the pages; it exists only for such callers.
+ *
+ * Same arguments and results as attn_bwd, without the workspace: the library uses its
+ * own fixed 64 MiB device array instead (held by every GPU that loads the library until
+ * the process exits).  Sizes whose attn_bwd_workspace_size exceeds 64 MiB are rejected
+ * with ATTN_ERR_WORKSPACE and a message in attn_last_error().  Nothing is allocated.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.  All calls
+ * share the array and it keeps the last call's contents (the backward clears what must
+ * start at zero itself), so calls that overlap on the GPU, e.g. on two streams, race.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                     int causal, float scale, int deterministic, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* attn_last_error(void);
 
