@@ -60,7 +60,7 @@ enum {
   B_PFULL = 3,    // +t
   B_STATS = 5,    // +t
   B_OREADY = 7,   // +t
-  B_OFULL = 9,    // +t
+  B_OFULL = 9,    // +t: the tile's last PV product has completed (one phase)
   B_DONE = 11,
   B_FULL = 12,    // +slot (up to 8)
   B_EMPTY = 20,   // +slot
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_o);
       const uint32_t qbytes = (T.n[0] > 0 ? C::TILE : 0) + (T.n[1] > 0 ? C::TILE : 0);
       mbar_arrive_expect_tx(BAR(B_Q), qbytes);
+#pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (T.n[t] == 0) continue;
         for (int c = 0; c < C::NCH; ++c)
@@ -255,8 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + D};
       bool ok = mbar_wait(BAR(B_Q), 0, wc);
       tc_fence_after();
       for (int j = 0; j <= nmax && ok; ++j) {
@@ -267,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t kbase = sbase + C::OFF_RING + kslot * C::TILE;
         const uint32_t vbase = sbase + C::OFF_RING + vslot * C::TILE;
-        for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          const uint32_t tS = tmem + uint32_t(t * 128), tO = tmem + 256u + uint32_t(t * D);
           if (j >= 1 && j <= T.n[t]) {
             // O_t += P_t(j-1) V_(j-1): needs the softmax's P and the correction's go-ahead.
             if (!mbar_wait(BAR(B_PFULL + t), (j - 1) & 1, wc) || !mbar_wait(BAR(B_OREADY + t), (j - 1) & 1, wc)) {
@@ -278,9 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024);
-              mma_ts(tO[t], tS[t] + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
+              mma_ts(tO, tS + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(BAR(B_OFULL + t));
+            // Only the tile's last PV is signalled here (for the epilogue).  The correction
+            // group learns that PV_t(j-1) finished from S_t(j)'s completion instead: MMAs
+            // complete in issue order.
+            if (j == T.n[t]) mma_commit(BAR(B_OFULL + t));
           }
           if (j < T.n[t]) {
             // S_t = Q_t K_j^T
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tS[t], sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
+              mma_ss(tS, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
                      kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(B_SFULL + t));
@@ -311,10 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = wg - 1;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + uint32_t(t * 128);
-    const int grow = T.row0[t] + row;
+    const int row0_t = t ? T.row0[1] : T.row0[0];
+    const int grow = row0_t + row;
     const float c = p.c;
     float m = -INFINITY, l = 0.f, lq = 0.f;
-    const int n_t = T.n[t];
+    const int n_t = t ? T.n[1] : T.n[0];
     for (int j = 0; j < n_t; ++j) {
       if (!warp_wait(BAR(B_SFULL + t), j & 1, wc)) break;
       tc_fence_after();
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence(u);
       float* s = reinterpret_cast<float*>(u);
       const int kb = j * 128;
-      const bool need_mask = (kb + 127 >= p.N) || (p.causal && kb + 127 > T.row0[t]);
+      const bool need_mask = (kb + 127 >= p.N) || (p.causal && kb + 127 > row0_t);
       if (need_mask) {
         const int lim = (p.causal ? min(grow, p.N - 1) : p.N - 1) - kb;  // last visible column
 #pragma unroll
@@ -353,11 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       alpha_buf[t * 128 + row] = alpha;
       mbar_arrive(BAR(B_STATS + t));
-      // p = 2^(s*c - m).  Two running sums: l over the fp32 p (for LSE) and lq over the
-      // bf16-rounded p the PV product actually uses (for O / lq, which makes a row whose
-      // weight sits on one key come out exact up to the output rounding).
+      // p = 2^(s*c - m).  l sums the fp32 p (it gives LSE).  O is divided by lq = l minus
+      // the bf16 rounding error of each block's largest p: when a row's weight sits on one
+      // key and the maximum is stale (that p is not exactly 1), the PV product uses
+      // bf16(p), and dividing by the matching sum makes O exact up to the output rounding.
       const float neg_m = -m;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accq[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 128; i += 2) {
@@ -365,15 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ffma2_bc(x0, x1, s[i], s[i + 1], c, neg_m);
         const float e0 = poly_lane<POLY>(i) ? exp2_poly(x0) : ex2_mufu(x0);
         const float e1 = poly_lane<POLY>(i + 1) ? exp2_poly(x1) : ex2_mufu(x1);
-        const uint32_t pr = pack_bf16x2(e0, e1);
-        pk[i >> 1] = pr;
+        pk[i >> 1] = pack_bf16x2(e0, e1);
         const int a2 = ((i >> 1) & 1) * 2;
         fadd2(acc[a2], acc[a2 + 1], acc[a2], acc[a2 + 1], e0, e1);
-        fadd2(accq[a2], accq[a2 + 1], accq[a2], accq[a2 + 1], __uint_as_float(pr << 16),
-              __uint_as_float(pr & 0xffff0000u));
       }
-      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      lq = lq * alpha + ((accq[0] + accq[1]) + (accq[2] + accq[3]));
+      {
+        const float pmax = ex2_mufu(fmaf(rmax, c, neg_m));   // bit-identical to that element's p above
+        const float pmax_q = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+        const float blk = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        l = l * alpha + blk;
+        lq = lq * alpha + (blk - (pmax - pmax_q));
+      }
       tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
@@ -393,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     bool ok = true;
     for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (j >= T.n[t]) continue;
+        if (!ok || j >= T.n[t]) continue;
         if (!warp_wait(BAR(B_STATS + t), j & 1, wc)) { ok = false; break; }
         const float alpha = alpha_buf[t * 128 + row];
         const bool any = __any_sync(0xffffffffu, alpha != 1.f);
@@ -403,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && bal) atomicAdd(p.rescale_count, (unsigned long long)__popc(bal));
         }
         if (j > 0 && any) {
-          if (!warp_wait(BAR(B_OFULL + t), (j - 1) & 1, wc)) { ok = false; break; }
+          // S_t(j) complete => PV_t(j-1), issued before it, is complete too.
+          if (!warp_wait(BAR(B_SFULL + t), j & 1, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
           uint32_t r[32];
@@ -424,11 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Epilogue per tile: O / l -> bf16 -> swizzled shared memory (the tile's Q buffer,
     // free once its last MMA completed) -> TMA store; LSE straight to global memory.
-    for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
       const int n_t = T.n[t];
-      if (n_t == 0) continue;
+      if (!ok || n_t == 0) continue;
       if (!warp_wait(BAR(B_FIN + t), 0, wc)) { ok = false; break; }
-      if (!warp_wait(BAR(B_OFULL + t), (n_t - 1) & 1, wc)) { ok = false; break; }
+      if (!warp_wait(BAR(B_OFULL + t), 0, wc)) { ok = false; break; }
       tc_fence_after();
       const float mrow = m_fin[t * 128 + row], lrow = l_fin[t * 128 + row];
       const float inv = 1.f / lq_fin[t * 128 + row];
