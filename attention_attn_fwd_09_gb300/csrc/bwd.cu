@@ -236,9 +236,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
 
+  // Query tiles are visited in a staggered order: key block n starts at query tile n, so
+  // the CTAs of one head add into different dQ rows at any moment (they would otherwise
+  // all hit the same rows together).  Causal CTAs already start at their diagonal tile.
+  // In deterministic mode each CTA still trails its predecessor by about one iteration.
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
-    m = m0 + it % n_m;
+    m = a.causal ? m0 + it % n_m : (it % n_m + n) % n_m;
     bh = b * a.Hq + hkv * a.g + r;
   };
 

@@ -339,15 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
+      // Row maximum over exactly the 128 columns: 4 seeds, 15 steps of 8, a last step of 4.
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 4; i < 128; i += 8) {
+      for (int i = 4; i < 124; i += 8) {
         mx[0] = fmax3(mx[0], s[i], s[i + 1]);
         mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
         mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
-        if (i + 7 < 128) mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
-        else mx[3] = fmaxf(mx[3], s[i + 6]);
+        mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
       }
+      mx[0] = fmax3(mx[0], s[124], s[125]);
+      mx[1] = fmax3(mx[1], s[126], s[127]);
       const float rmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       const float m_cand = fmaxf(m, rmax * c);
       float alpha = 1.f;

@@ -172,3 +172,18 @@ def test_bounded_wait_gives_up_cleanly(A):
     o, lse = run(A, x, False, 0.1)
     O, L = oracle.attn_fwd(x["q"], x["k"], x["v"], False, 0.1)
     check_fwd(o, lse, O, L, "after timeout")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_is_exact(A, d, causal):
+    # With one key every probability is exactly 1, so O must be V bit for bit (any error
+    # in the row maximum or the normaliser shows up as a one-ulp change) and LSE the score.
+    B, Hq, Hkv = 2, 4, 2
+    x = make_inputs(600 + d, B, Hq, Hkv, 1, d)
+    scale = default_scale(d)
+    o, lse = run(A, x, causal, scale)
+    v = x["v"].float().numpy().repeat(Hq // Hkv, axis=1)
+    assert np.array_equal(o, v)
+    s = (x["q"].double() * x["k"].double().repeat_interleave(Hq // Hkv, dim=1)).sum(-1).numpy() * scale
+    np.testing.assert_allclose(lse, s, rtol=0, atol=1e-5)
