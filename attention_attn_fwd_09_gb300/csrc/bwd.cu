@@ -12,8 +12,8 @@
 //                 dS^T = P^T o (dP^T - D)      (bf16, to shared memory)
 //                 dK  += dS^T Q                (A = dS^T, K-major view of the tile)
 //                 dQ   = dS K                  (A = dS, MN-major view of the same tile)
-//                 dQacc += dQ                  (fp32 atomics, or in key-block order when
-//                                               deterministic)
+//                 dQacc += dQ                  (fp32 TMA bulk reductions; in key-block order
+//                                               when deterministic)
 //               The transposed orientation (keys on TMEM lanes) makes every result land in
 //               the layout its consumer reads ("FlashAttention-4 explained" section 05).
 //   convert     dq = bf16(scale * dQacc)
@@ -149,7 +149,9 @@ struct BwdCfg {
 
 enum {
   W_KV = 0, W_FULL = 1 /* +stage */, W_EMPTY = 3 /* +stage */, W_S = 5, W_DP = 6, W_P = 7, W_DS = 8, W_DQ = 9,
-  W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15, W_COUNT = 16
+  W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15,
+  W_DSBUF = 16,   // the drain has finished staging dQ in the dS buffer (one arrival)
+  W_COUNT = 17
 };
 
 // Bounded barrier for one warpgroup (128 threads) built on an mbarrier: every thread
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                    const BwdKernelArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dqacc, const BwdKernelArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
       mbar_init(BAR(i), (i == W_P || i == W_DS || i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GD) ? 128 : 1);
+    // W_DSBUF: one arrival (the drain's leader) per iteration.
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -386,8 +389,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(W_P));
-      // dS^T = P^T o (dP^T - D), bf16, into the shared tile (rows = keys, 128B swizzle).
-      if (it > 0 && !warp_wait_b(BAR(W_DSFREE), (it - 1) & 1, wc)) { ok = false; break; }
+      // dS^T = P^T o (dP^T - D), bf16, into the shared tile (rows = keys, 128B swizzle),
+      // once the previous dK/dQ products and the drain's use of the buffer are over.
+      if (it > 0 && (!warp_wait_b(BAR(W_DSFREE), (it - 1) & 1, wc) || !warp_wait_b(BAR(W_DSBUF), (it - 1) & 1, wc))) {
+        ok = false;
+        break;
+      }
       if (!warp_wait_b(BAR(W_DP), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -457,8 +464,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------------ drain: dQ -> dQacc
+    // dQ leaves TMEM into registers (the columns are then free for the next dP), is staged
+    // 64 columns at a time in the dS buffer (two 128-row x 32-column fp32 boxes, 128-byte
+    // swizzle) and added into dQacc by TMA bulk reductions, which move whole lines.
     const int row = (warp & 3) * 32 + lane;          // query row within the tile
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const bool leader = warp == 8 && lane == 0;
+    uint8_t* stage = smem + C::OFF_DS;
     bool ok = true;
     int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
@@ -468,27 +480,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       float v[D];
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t r[32];
-        tmem_ld32(tdP + lane_off + q * 32, r);
-        tmem_wait_ld();
-        reg_fence_b(r);
+      for (int q = 0; q < D / 32; ++q) tmem_ld32(tdP + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[q * 32]));
+      tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[q * 32 + i] = __uint_as_float(r[i]);
-      }
+      for (int i = 0; i < D; ++i) asm volatile("" : "+f"(v[i])::"memory");
       tc_fence_before();
       mbar_arrive(BAR(W_DQFREE));
-      const int qrow = m * 128 + row;
-      float* dst = a.dq_acc + ((size_t)bh * a.N + qrow) * D;
-      if (!a.deterministic) {
-        if (qrow < a.N) {
-#pragma unroll
-          for (int c = 0; c < D; c += 4) red_add_v4(dst + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
-        }
-      } else {
+      int* sem = a.deterministic ? a.sem + (size_t)bh * a.nq + m : nullptr;
+      if (a.deterministic) {
         // Contributions to this query tile are added in key-block order 0, 1, 2, ...
-        int* sem = a.sem + (size_t)bh * a.nq + m;
-        if (warp == 8 && lane == 0) {
+        if (leader) {
           const unsigned long long t0 = globaltimer_ns();
           while (ld_acquire(sem) != n) {
             if (*abort_flag) break;
@@ -500,19 +501,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
-        if (qrow < a.N) {
+      }
 #pragma unroll
-          for (int c = 0; c < D; c += 4) {
-            float4 x = __ldcg(reinterpret_cast<const float4*>(dst + c));
-            x.x += v[c]; x.y += v[c + 1]; x.z += v[c + 2]; x.w += v[c + 3];
-            __stcg(reinterpret_cast<float4*>(dst + c), x);
-          }
+      for (int half = 0; half < D / 64; ++half) {
+        if (half > 0) {
+          if (leader) tma_store_wait_read();
+          if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
         }
-        __threadfence();
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+          const float* src = &v[half * 64 + bx * 32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
+                make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
         if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
-        if (warp == 8 && lane == 0) atomicAdd(sem, 1);
+        if (leader) {
+          tma_reduce_add_3d(&tm_dqacc, smem_u32(stage), half * 64, m * 128, bh);
+          tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + 16384), half * 64 + 32, m * 128, bh);
+          tma_store_commit();
+        }
+      }
+      if (!ok) break;
+      if (leader) {
+        if (a.deterministic) {
+          tma_store_wait_all();                       // the adds have landed
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          atomicAdd(sem, 1);
+        } else {
+          tma_store_wait_read();                      // the staging buffer has been read
+        }
+        mbar_arrive(BAR(W_DSBUF));
       }
     }
+    if (leader) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -557,7 +582,7 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
     const long long grid = (long long)p.B * p.Hkv * nq;
-    kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
+    kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dqacc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -55,6 +55,7 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dout, dk, dv;
+  CUtensorMap dqacc;   // fp32 [B*Hq, N, d], boxes of 128 rows x 32 columns, 128-byte swizzle
 };
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic);
