@@ -150,7 +150,7 @@ struct BwdCfg {
 enum {
   W_KV = 0, W_FULL = 1 /* +stage */, W_EMPTY = 3 /* +stage */, W_S = 5, W_DP = 6, W_P = 7, W_DS = 8, W_DQ = 9,
   W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15,
-  W_DSBUF = 16,   // the drain has finished staging dQ in the dS buffer (one arrival)
+  W_DRAINED = 16, // the drain warpgroup has finished (one arrival)
   W_COUNT = 17
 };
 
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
       mbar_init(BAR(i), (i == W_P || i == W_DS || i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GD) ? 128 : 1);
-    // W_DSBUF: one arrival (the drain's leader) per iteration.
+    // W_EMPTY: released by the drain's leader (one arrival), W_DRAINED: one arrival.
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -329,8 +329,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tdP, sdesc_sw128(dsb + kk * 2048, C::CHUNK, 1024), sdesc_sw128(kb + kk * 2048, C::CHUNK, 1024),
                  C::IDESC_DQ, kk > 0);
-        mma_commit(BAR(W_DQ));
-        mma_commit(BAR(W_EMPTY + st));
+        mma_commit(BAR(W_DQ));          // the drain releases this Q/dO stage after staging dQ in it
         mma_commit(BAR(W_DSFREE));
       }
       mma_commit(BAR(W_DONE));
@@ -349,13 +348,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int it = 0; it < n_iter && ok; ++it) {
       int bh, m;
       iter_head_row(it, bh, m);
-      // Stage this query tile's LSE2 and D (row index = query within the tile); the first
-      // sync keeps the previous tile's readers ahead of the overwrite.
+      // Stage this query tile's -LSE2 and -D (row index = query within the tile); the first
+      // sync keeps the previous tile's readers ahead of the overwrite.  Queries past N get
+      // -inf / 0, which makes their probabilities and dS exactly zero.
       if (!group_sync(BAR(W_GC), gphase, wc)) { ok = false; break; }
       {
         const int qj = m * 128 + row;
-        vec_lse[row] = qj < a.N ? a.lse2[(size_t)bh * a.N + qj] : INFINITY;
-        vec_d[row] = qj < a.N ? a.delta[(size_t)bh * a.N + qj] : 0.f;
+        vec_lse[row] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
+        vec_d[row] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
       }
       if (!group_sync(BAR(W_GC), gphase, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_S), it & 1, wc)) { ok = false; break; }
@@ -363,68 +363,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Visible queries for this key row: qj >= kr when causal, qj < N, and the key itself < N.
       const int qmin = a.causal ? kr - m * 128 : 0;          // columns below qmin are masked
       const bool key_ok = kr < a.N;
+      const bool need_mask = qmin > 0 || !key_ok;
+      const float4* nl4 = reinterpret_cast<const float4*>(vec_lse);
+      const float4* nd4 = reinterpret_cast<const float4*>(vec_d);
       uint32_t pk[64];
+      {
+        uint32_t u[128];
 #pragma unroll
-      for (int cch = 0; cch < 4; ++cch) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + cch * 32, r);
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[q * 32]));
         tmem_wait_ld();
-        reg_fence_b(r);
+        reg_fence_b(u);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int c0 = cch * 32 + i;
-          float p0 = ex2_mufu(fmaf(__uint_as_float(r[i]), a.c, -vec_lse[c0]));
-          float p1 = ex2_mufu(fmaf(__uint_as_float(r[i + 1]), a.c, -vec_lse[c0 + 1]));
-          if (c0 < qmin || !key_ok) p0 = 0.f;
-          if (c0 + 1 < qmin || !key_ok) p1 = 0.f;
-          pk[c0 / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 128; i += 4) {
+          const float4 nl = nl4[i >> 2];
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(u[i]), __uint_as_float(u[i + 1]), a.c, a.c, nl.x, nl.y);
+          ffma2(x2, x3, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]), a.c, a.c, nl.z, nl.w);
+          float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1), p2 = ex2_mufu(x2), p3 = ex2_mufu(x3);
+          if (need_mask) {
+            if (i < qmin || !key_ok) p0 = 0.f;
+            if (i + 1 < qmin || !key_ok) p1 = 0.f;
+            if (i + 2 < qmin || !key_ok) p2 = 0.f;
+            if (i + 3 < qmin || !key_ok) p3 = 0.f;
+          }
+          pk[i >> 1] = pack_bf16x2(p0, p1);
+          pk[(i >> 1) + 1] = pack_bf16x2(p2, p3);
         }
       }
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-        tmem_st32(tS + lane_off, lo);
-        tmem_st32(tS + lane_off + 32, hi);
-      }
+      tmem_st32(tS + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(W_P));
       // dS^T = P^T o (dP^T - D), bf16, into the shared tile (rows = keys, 128B swizzle),
-      // once the previous dK/dQ products and the drain's use of the buffer are over.
-      if (it > 0 && (!warp_wait_b(BAR(W_DSFREE), (it - 1) & 1, wc) || !warp_wait_b(BAR(W_DSBUF), (it - 1) & 1, wc))) {
-        ok = false;
-        break;
-      }
+      // once the previous dK/dQ products have finished reading it.
+      if (it > 0 && !warp_wait_b(BAR(W_DSFREE), (it - 1) & 1, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_DP), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int cch = 0; cch < 4; ++cch) {
-        uint32_t r[32];
-        tmem_ld32(tdP + lane_off + cch * 32, r);
+      for (int hh = 0; hh < 2; ++hh) {      // two halves of 64 columns keep the live set small
+        uint32_t u[64];
+        tmem_ld32(tdP + lane_off + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tdP + lane_off + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        reg_fence_b(r);
-        uint32_t out[16];
+        reg_fence_b(u);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int c0 = cch * 32 + i;
-          const uint32_t pp = pk[c0 / 2];
-          const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
-          out[i / 2] = pack_bf16x2(p0 * (__uint_as_float(r[i]) - vec_d[c0]),
-                                   p1 * (__uint_as_float(r[i + 1]) - vec_d[c0 + 1]));
-        }
-        const int box = cch >> 1, j0 = (cch & 1) * 4;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int cch = hh * 2 + cc;
+          uint32_t out[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t off = box * C::CHUNK + row * 128 + (((j0 + u) ^ (row & 7)) * 16);
-          *reinterpret_cast<uint4*>(ds_tile + off) = make_uint4(out[4 * u], out[4 * u + 1], out[4 * u + 2], out[4 * u + 3]);
+          for (int i = 0; i < 32; i += 4) {
+            const int c0 = cch * 32 + i, l0 = cc * 32 + i;
+            const float4 nd = nd4[c0 >> 2];
+            const uint32_t pa = pk[c0 >> 1], pb = pk[(c0 >> 1) + 1];
+            float e0, e1, e2, e3;
+            fadd2(e0, e1, __uint_as_float(u[l0]), __uint_as_float(u[l0 + 1]), nd.x, nd.y);
+            fadd2(e2, e3, __uint_as_float(u[l0 + 2]), __uint_as_float(u[l0 + 3]), nd.z, nd.w);
+            fmul2(e0, e1, e0, e1, __uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u));
+            fmul2(e2, e3, e2, e3, __uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u));
+            out[i >> 1] = pack_bf16x2(e0, e1);
+            out[(i >> 1) + 1] = pack_bf16x2(e2, e3);
+          }
+          const int box = cch >> 1, j0 = (cch & 1) * 4;
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu) {
+            const uint32_t off = box * C::CHUNK + row * 128 + (((j0 + uu) ^ (row & 7)) * 16);
+            *reinterpret_cast<uint4*>(ds_tile + off) =
+                make_uint4(out[4 * uu], out[4 * uu + 1], out[4 * uu + 2], out[4 * uu + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(BAR(W_DS));
     }
-    // Epilogue: dV and scale * dK -> bf16 -> stage 0 buffers -> TMA store.
-    if (ok && warp_wait_b(BAR(W_DONE), 0, wc)) {
+    // Epilogue: dV and scale * dK -> bf16 -> stage 0 buffers -> TMA store, once every MMA
+    // has completed and the drain no longer stages dQ in the stage buffers.
+    if (ok && warp_wait_b(BAR(W_DONE), 0, wc) && warp_wait_b(BAR(W_DRAINED), 0, wc)) {
       tc_fence_after();
       uint8_t* sv = smem + C::OFF_STAGE;
       uint8_t* sk = sv + C::TILE;
@@ -465,17 +480,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------------------------ drain: dQ -> dQacc
     // dQ leaves TMEM into registers (the columns are then free for the next dP), is staged
-    // 64 columns at a time in the dS buffer (two 128-row x 32-column fp32 boxes, 128-byte
-    // swizzle) and added into dQacc by TMA bulk reductions, which move whole lines.
+    // in this iteration's Q/dO stage buffer (its MMAs are done; the producer refills it
+    // only for the iteration after next, once the drain releases it) as 128-row x
+    // 32-column fp32 boxes with 128-byte swizzle, and is added into dQacc by TMA bulk
+    // reductions, which move whole lines.
     const int row = (warp & 3) * 32 + lane;          // query row within the tile
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const bool leader = warp == 8 && lane == 0;
-    uint8_t* stage = smem + C::OFF_DS;
     bool ok = true;
     int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
       int bh, m;
       iter_head_row(it, bh, m);
+      const int st = it & 1;
+      uint8_t* stage = smem + C::OFF_STAGE + st * 2 * C::TILE;
       if (!warp_wait_b(BAR(W_DQ), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float v[D];
@@ -503,41 +521,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
       }
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        if (half > 0) {
-          if (leader) tma_store_wait_read();
-          if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
-        }
+      for (int bx = 0; bx < D / 32; ++bx) {
+        const float* src = &v[bx * 32];
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
-          const float* src = &v[half * 64 + bx * 32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
-                make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
-        }
-        fence_proxy_async_smem();
-        if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
-        if (leader) {
-          tma_reduce_add_3d(&tm_dqacc, smem_u32(stage), half * 64, m * 128, bh);
-          tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + 16384), half * 64 + 32, m * 128, bh);
-          tma_store_commit();
-        }
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
+              make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
       }
-      if (!ok) break;
+      fence_proxy_async_smem();
+      if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
       if (leader) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + bx * 16384), bx * 32, m * 128, bh);
+        tma_store_commit();
         if (a.deterministic) {
           tma_store_wait_all();                       // the adds have landed
           asm volatile("fence.proxy.async.global;" ::: "memory");
           __threadfence();
           atomicAdd(sem, 1);
         } else {
-          tma_store_wait_read();                      // the staging buffer has been read
+          tma_store_wait_read();                      // the stage buffer has been read
         }
-        mbar_arrive(BAR(W_DSBUF));
+        mbar_arrive(BAR(W_EMPTY + st));
       }
     }
-    if (leader) tma_store_wait_all();
+    if (leader) {
+      tma_store_wait_all();
+      mbar_arrive(BAR(W_DRAINED));
+    }
   }
 
   tc_fence_before();
