@@ -59,11 +59,10 @@ enum {
   B_SFULL = 1,    // +t
   B_PFULL = 3,    // +t
   B_STATS = 5,    // +t
-  B_OREADY = 7,   // +t
+  B_REL = 7,      // +(group & 1): K/V slots of release group j (K_j, V_(j-1)) are free
   B_OFULL = 9,    // +t: the tile's last PV product has completed (one phase)
   B_DONE = 11,
   B_FULL = 12,    // +slot (up to 8)
-  B_EMPTY = 20,   // +slot
   B_EPI = 28,     // +t: the tile's O rows are staged in shared memory
   B_FIN = 30,     // +t: final row statistics (m, l) written (one phase only)
   B_COUNT = 32
@@ -174,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_Q), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(B_SFULL + t), 1);
-      mbar_init(BAR(B_PFULL + t), 128);
+      mbar_init(BAR(B_PFULL + t), 256);   // softmax (P written) + correction (O rescaled)
       mbar_init(BAR(B_STATS + t), 128);
-      mbar_init(BAR(B_OREADY + t), 128);
+      mbar_init(BAR(B_REL + t), 1);
       mbar_init(BAR(B_OFULL + t), 1);
     }
     mbar_init(BAR(B_DONE), 1);
@@ -184,10 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_EPI + 1), 128);
     mbar_init(BAR(B_FIN + 0), 128);
     mbar_init(BAR(B_FIN + 1), 128);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(BAR(B_FULL + s), 1);
-      mbar_init(BAR(B_EMPTY + s), 1);
-    }
+    for (int s = 0; s < C::NS; ++s) mbar_init(BAR(B_FULL + s), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -227,10 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j < nmax && ok; ++j) {
         for (int which = 0; which < 2; ++which) {
-          const int idx = 2 * j + which, slot = idx % C::NS, round = idx / C::NS;
-          if (round > 0 && !mbar_wait(BAR(B_EMPTY + slot), (round - 1) & 1, wc)) {
-            ok = false;
-            break;
+          const int idx = 2 * j + which, slot = idx % C::NS;
+          if (idx >= C::NS) {
+            // The slot's previous occupant (ring index idx - NS) is released with group g.
+            const int g = (idx - C::NS + 1) / 2;
+            if (!mbar_wait(BAR(B_REL + (g & 1)), (g >> 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
           }
           next_idx = idx + 1;
           if (idx == skip_idx) continue;
@@ -271,8 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           const uint32_t tS = tmem + uint32_t(t * 128), tO = tmem + 256u + uint32_t(t * D);
           if (j >= 1 && j <= T.n[t]) {
-            // O_t += P_t(j-1) V_(j-1): needs the softmax's P and the correction's go-ahead.
-            if (!mbar_wait(BAR(B_PFULL + t), (j - 1) & 1, wc) || !mbar_wait(BAR(B_OREADY + t), (j - 1) & 1, wc)) {
+            // O_t += P_t(j-1) V_(j-1): the P barrier also carries the correction group's
+            // arrival (O rescaled, or no rescale needed).
+            if (!mbar_wait(BAR(B_PFULL + t), (j - 1) & 1, wc)) {
               ok = false;
               break;
             }
@@ -300,8 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (j < nmax) mma_commit(BAR(B_EMPTY + kslot));
-        if (j >= 1) mma_commit(BAR(B_EMPTY + vslot));
+        mma_commit(BAR(B_REL + (j & 1)));   // releases K_j and V_(j-1) together
       }
       // Drain: every MMA issued above completes before TMEM is released.
       mma_commit(BAR(B_DONE));
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(BAR(B_OREADY + t));
+        mbar_arrive(BAR(B_PFULL + t));
       }
     }
     // Epilogue per tile: O / l -> bf16 -> swizzled shared memory (the tile's Q buffer,
