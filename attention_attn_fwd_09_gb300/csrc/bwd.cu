@@ -249,6 +249,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bh = b * a.Hq + hkv * a.g + r;
   };
 
+  // Register split (per thread): warpgroup 0 (producer, MMA) 56, compute 232, drain 216:
+  // 56 + 232 + 216 = 504 = 3 x 168, the launch's 168 x 384 threads.  Each role's code sits
+  // inside its own branch so that its limit covers it.
+  const int wg = warp >> 2;
+  if (wg == 0) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
@@ -337,7 +343,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       while (!mbar_try_wait(BAR(W_DONE), 0) && globaltimer_ns() - t0 < a.wait_ns) {
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  }
+  } else if (wg == 1) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
     // ------------------------------------------------------------------ compute: P^T, dS^T
     const int row = (warp & 3) * 32 + lane;          // key row within the block
     const int kr = n * 128 + row;
@@ -477,7 +485,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_store_wait_all();
       }
     }
-  } else if (warp >= 8) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------------ drain: dQ -> dQacc
     // dQ leaves TMEM into registers (the columns are then free for the next dP), is staged
     // in this iteration's Q/dO stage buffer (its MMAs are done; the producer refills it
