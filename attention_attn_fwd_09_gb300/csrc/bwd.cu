@@ -124,10 +124,11 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 // ------------------------------------------------------------------------------------
 // Main backward kernel.
 // Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle,
-//        4-7 "compute" (P^T, dS^T; keys on TMEM lanes), 8-11 "drain" (dQ rows -> dQacc).
+//        4-7 and 8-11 "compute" (P^T, dS^T; keys on TMEM lanes; queries 0-63 and 64-127),
+//        12-15 "drain" (dQ rows -> dQacc).
 // TMEM columns: S^T/P^T [0,128), dP^T then dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 // ------------------------------------------------------------------------------------
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 
 template <int D>
 struct BwdCfg {
@@ -151,7 +152,8 @@ enum {
   W_KV = 0, W_FULL = 1 /* +stage */, W_EMPTY = 3 /* +stage */, W_S = 5, W_DP = 6, W_P = 7, W_DS = 8, W_DQ = 9,
   W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15,
   W_DRAINED = 16, // the drain warpgroup has finished (one arrival)
-  W_COUNT = 17
+  W_GC1 = 17,     // staging sync of the second compute warpgroup
+  W_COUNT = 18
 };
 
 // Bounded barrier for one warpgroup (128 threads) built on an mbarrier: every thread
@@ -224,7 +226,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
-      mbar_init(BAR(i), (i == W_P || i == W_DS || i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GD) ? 128 : 1);
+      mbar_init(BAR(i), (i == W_P || i == W_DS) ? 256
+                        : (i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GC1 || i == W_GD) ? 128 : 1);
     // W_EMPTY: released by the drain's leader (one arrival), W_DRAINED: one arrival.
     *abort_flag = 0;
     fence_mbar_init();
@@ -249,9 +252,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bh = b * a.Hq + hkv * a.g + r;
   };
 
-  // Register split (per thread): warpgroup 0 (producer, MMA) 56, compute 232, drain 216:
-  // 56 + 232 + 216 = 504 = 3 x 168, the launch's 168 x 384 threads.  Each role's code sits
-  // inside its own branch so that its limit covers it.
+  // Register split (per thread): warpgroup 0 (producer, MMA) 56, two compute warpgroups
+  // 152 each, drain 152: 56 + 3 x 152 = 512 = 4 x 128, the launch's 128 x 512 threads.  Each
+  // role's code sits inside its own branch so that its limit covers it.
   const int wg = warp >> 2;
   if (wg == 0) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
@@ -321,7 +324,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdV, tS + kk * 8, sdesc_sw128(dos + kk * 2048, C::CHUNK, 1024), C::IDESC_KB, (it > 0 || kk > 0));
+          mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dos + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
+                 (it > 0 || kk > 0));
         // dK += dS^T Q ; dQ = dS K
         if (!mbar_wait(BAR(W_DS), it & 1, wc)) { ok = false; break; }
         tc_fence_after();
@@ -344,9 +348,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
-  } else if (wg == 1) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+  } else if (wg == 1 || wg == 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------------ compute: P^T, dS^T
+    // Two warpgroups share the work column-wise: half h owns queries [64h, 64h + 64) of
+    // every key row.  Its packed P goes to TMEM columns [64h, 64h + 32), inside its own
+    // part of S, so neither half overwrites scores the other has not read yet.
+    const int h = wg - 1;
     const int row = (warp & 3) * 32 + lane;          // key row within the block
     const int kr = n * 128 + row;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
@@ -356,33 +364,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int it = 0; it < n_iter && ok; ++it) {
       int bh, m;
       iter_head_row(it, bh, m);
-      // Stage this query tile's -LSE2 and -D (row index = query within the tile); the first
-      // sync keeps the previous tile's readers ahead of the overwrite.  Queries past N get
-      // -inf / 0, which makes their probabilities and dS exactly zero.
-      if (!group_sync(BAR(W_GC), gphase, wc)) { ok = false; break; }
-      {
-        const int qj = m * 128 + row;
-        vec_lse[row] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
-        vec_d[row] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
+      // Stage this half's -LSE2 and -D (index = query within the tile); the first sync keeps
+      // the previous tile's readers ahead of the overwrite.  Queries past N get -inf / 0,
+      // which makes their probabilities and dS exactly zero.
+      if (!group_sync(BAR(h ? W_GC1 : W_GC), gphase, wc)) { ok = false; break; }
+      if (row < 64) {
+        const int qc = h * 64 + row, qj = m * 128 + qc;
+        vec_lse[qc] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
+        vec_d[qc] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
       }
-      if (!group_sync(BAR(W_GC), gphase, wc)) { ok = false; break; }
+      if (!group_sync(BAR(h ? W_GC1 : W_GC), gphase, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_S), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
       // Visible queries for this key row: qj >= kr when causal, qj < N, and the key itself < N.
-      const int qmin = a.causal ? kr - m * 128 : 0;          // columns below qmin are masked
+      const int qmin = (a.causal ? kr - m * 128 : 0) - h * 64;   // this half's columns below qmin are masked
       const bool key_ok = kr < a.N;
       const bool need_mask = qmin > 0 || !key_ok;
-      const float4* nl4 = reinterpret_cast<const float4*>(vec_lse);
-      const float4* nd4 = reinterpret_cast<const float4*>(vec_d);
-      uint32_t pk[64];
+      const float4* nl4 = reinterpret_cast<const float4*>(vec_lse + h * 64);
+      const float4* nd4 = reinterpret_cast<const float4*>(vec_d + h * 64);
+      uint32_t pk[32];
       {
-        uint32_t u[128];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[q * 32]));
+        uint32_t u[64];
+        tmem_ld32(tS + lane_off + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
         reg_fence_b(u);
 #pragma unroll
-        for (int i = 0; i < 128; i += 4) {
+        for (int i = 0; i < 64; i += 4) {
           const float4 nl = nl4[i >> 2];
           float x0, x1, x2, x3;
           ffma2(x0, x1, __uint_as_float(u[i]), __uint_as_float(u[i + 1]), a.c, a.c, nl.x, nl.y);
@@ -398,8 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[(i >> 1) + 1] = pack_bf16x2(p2, p3);
         }
       }
-      tmem_st32(tS + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st32(tS + lane_off + h * 64, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(W_P));
@@ -408,22 +415,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it > 0 && !warp_wait_b(BAR(W_DSFREE), (it - 1) & 1, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_DP), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {      // two halves of 64 columns keep the live set small
+      {
         uint32_t u[64];
-        tmem_ld32(tdP + lane_off + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tdP + lane_off + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_ld32(tdP + lane_off + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tdP + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
         reg_fence_b(u);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int cch = hh * 2 + cc;
           uint32_t out[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const int c0 = cch * 32 + i, l0 = cc * 32 + i;
-            const float4 nd = nd4[c0 >> 2];
-            const uint32_t pa = pk[c0 >> 1], pb = pk[(c0 >> 1) + 1];
+            const int l0 = cc * 32 + i;
+            const float4 nd = nd4[l0 >> 2];
+            const uint32_t pa = pk[l0 >> 1], pb = pk[(l0 >> 1) + 1];
             float e0, e1, e2, e3;
             fadd2(e0, e1, __uint_as_float(u[l0]), __uint_as_float(u[l0 + 1]), nd.x, nd.y);
             fadd2(e2, e3, __uint_as_float(u[l0 + 2]), __uint_as_float(u[l0 + 3]), nd.z, nd.w);
@@ -432,10 +437,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             out[i >> 1] = pack_bf16x2(e0, e1);
             out[(i >> 1) + 1] = pack_bf16x2(e2, e3);
           }
-          const int box = cch >> 1, j0 = (cch & 1) * 4;
+          // Query columns [64h + 32cc, +32) are 16-byte chunks 4cc..4cc+3 of box h.
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu) {
-            const uint32_t off = box * C::CHUNK + row * 128 + (((j0 + uu) ^ (row & 7)) * 16);
+            const uint32_t off = h * C::CHUNK + row * 128 + ((((cc * 4) + uu) ^ (row & 7)) * 16);
             *reinterpret_cast<uint4*>(ds_tile + off) =
                 make_uint4(out[4 * uu], out[4 * uu + 1], out[4 * uu + 2], out[4 * uu + 3]);
           }
@@ -447,7 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // Epilogue: dV and scale * dK -> bf16 -> stage 0 buffers -> TMA store, once every MMA
     // has completed and the drain no longer stages dQ in the stage buffers.
-    if (ok && warp_wait_b(BAR(W_DONE), 0, wc) && warp_wait_b(BAR(W_DRAINED), 0, wc)) {
+    if (h == 0 && ok && warp_wait_b(BAR(W_DONE), 0, wc) && warp_wait_b(BAR(W_DRAINED), 0, wc)) {
       tc_fence_after();
       uint8_t* sv = smem + C::OFF_STAGE;
       uint8_t* sk = sv + C::TILE;
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------------ drain: dQ -> dQacc
     // dQ leaves TMEM into registers (the columns are then free for the next dP), is staged
     // in this iteration's Q/dO stage buffer (its MMAs are done; the producer refills it
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // reductions, which move whole lines.
     const int row = (warp & 3) * 32 + lane;          // query row within the tile
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const bool leader = warp == 8 && lane == 0;
+    const bool leader = warp == 12 && lane == 0;
     bool ok = true;
     int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
