@@ -12,8 +12,11 @@
 //                 dS^T = P^T o (dP^T - D)      (bf16, to shared memory)
 //                 dK  += dS^T Q                (A = dS^T, K-major view of the tile)
 //                 dQ   = dS K                  (A = dS, MN-major view of the same tile)
-//                 dQacc += dQ                  (fp32 TMA bulk reductions; in key-block order
-//                                               when deterministic)
+//                 dQacc += dQ                  (CTA pairs on adjacent key blocks swap dQ
+//                                               halves through distributed shared memory;
+//                                               each adds the pair's sum for its half with
+//                                               fp32 TMA bulk reductions, in pair order when
+//                                               deterministic)
 //               The transposed orientation (keys on TMEM lanes) makes every result land in
 //               the layout its consumer reads ("FlashAttention-4 explained" section 05).
 //   convert     dq = bf16(scale * dQacc)
@@ -34,7 +37,7 @@ size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int determinist
   const size_t rows = (size_t)B * Hq * N;
   const size_t nq = (size_t)B * Hq * ((N + 127) / 128);
   size_t n = align256(rows * d * 4) + 2 * align256(rows * 4);
-  if (deterministic) n += align256(nq * 4);
+  if (deterministic) n += align256(nq * 2 * 4);   // one counter per (query tile, dQ half)
   return n;
 }
 
@@ -153,7 +156,9 @@ enum {
   W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15,
   W_DRAINED = 16, // the drain warpgroup has finished (one arrival)
   W_GC1 = 17,     // staging sync of the second compute warpgroup
-  W_COUNT = 18
+  X_READY = 18,   // +stage: the partner CTA's stage buffer may receive our dQ half (1 remote arrival)
+  X_RECV = 20,    // +stage: the partner's dQ half has landed in our stage buffer (128 remote arrivals)
+  W_COUNT = 22
 };
 
 // Bounded barrier for one warpgroup (128 threads) built on an mbarrier: every thread
@@ -188,7 +193,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 }
 
 struct BwdKernelArgs {
-  int B, Hq, Hkv, N, g, nq, nkb, causal, deterministic;
+  int B, Hq, Hkv, N, g, nq, nkb /* key blocks per head rounded up to even */, causal, deterministic;
   float c, scale;
   const float* lse2;
   const float* delta;
@@ -199,7 +204,7 @@ struct BwdKernelArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -217,17 +222,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* vec_d = vec_lse + 128;
 
   const int warp = warp_id(), lane = lane_id();
+  // The two CTAs of a cluster take adjacent key blocks n = 2p, 2p + 1 of one K/V head
+  // and visit the same query tiles in the same order.  When the head has an odd number
+  // of key blocks the last cluster's second CTA has no block ("dead"): it only joins the
+  // cluster barriers, and its partner adds its whole dQ by itself ("unpaired").
   const int bkv = blockIdx.x / a.nkb, n = blockIdx.x % a.nkb;
   const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
-  const int m0 = a.causal ? n : 0;
+  const uint32_t rank = cluster_ctarank();            // == n & 1
+  const int pair = n >> 1;
+  const bool live = n < a.nq;
+  const bool paired = (n | 1) < a.nq;
+  const int m0 = a.causal ? 2 * pair : 0;
   const int n_m = a.nq - m0;
-  const int n_iter = a.g * n_m;
+  const int n_iter = live ? a.g * n_m : 0;
   WaitCtl wc{a.wait_ns, a.status, abort_flag};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
       mbar_init(BAR(i), (i == W_P || i == W_DS) ? 256
-                        : (i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GC1 || i == W_GD) ? 128 : 1);
+                        : (i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GC1 || i == W_GD || i == X_RECV ||
+                           i == X_RECV + 1) ? 128 : 1);
     // W_EMPTY: released by the drain's leader (one arrival), W_DRAINED: one arrival.
     *abort_flag = 0;
     fence_mbar_init();
@@ -237,18 +251,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before either arrives on the other's
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
 
-  // Query tiles are visited in a staggered order: key block n starts at query tile n, so
-  // the CTAs of one head add into different dQ rows at any moment (they would otherwise
-  // all hit the same rows together).  Causal CTAs already start at their diagonal tile.
-  // In deterministic mode each CTA still trails its predecessor by about one iteration.
+  // Query tiles are visited in a staggered order: pair p starts at query tile p, so the
+  // pairs of one head add into different dQ rows at any moment (they would otherwise
+  // all hit the same rows together).  Causal pairs start at the diagonal tile of their
+  // first key block (for the second block that tile is fully masked).  In deterministic
+  // mode each pair still trails its predecessor by about one iteration.
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
-    m = a.causal ? m0 + it % n_m : (it % n_m + n) % n_m;
+    m = a.causal ? m0 + it % n_m : (it % n_m + pair) % n_m;
     bh = b * a.Hq + hkv * a.g + r;
   };
 
@@ -256,7 +271,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // 152 each, drain 152: 56 + 3 x 152 = 512 = 4 x 128, the launch's 128 x 512 threads.  Each
   // role's code sits inside its own branch so that its limit covers it.
   const int wg = warp >> 2;
-  if (wg == 0) {
+  if (!live) {
+    // no key block: nothing to compute
+  } else if (wg == 0) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -493,14 +510,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------------ drain: dQ -> dQacc
-    // dQ leaves TMEM into registers (the columns are then free for the next dP), is staged
-    // in this iteration's Q/dO stage buffer (its MMAs are done; the producer refills it
-    // only for the iteration after next, once the drain releases it) as 128-row x
-    // 32-column fp32 boxes with 128-byte swizzle, and is added into dQacc by TMA bulk
-    // reductions, which move whole lines.
+    // dQ leaves TMEM into registers (the columns are then free for the next dP).  A paired
+    // CTA keeps dQ columns [rank * D/2, rank * D/2 + D/2) and stores the other half of
+    // each row straight into its partner's stage buffer for this iteration (distributed
+    // shared memory), once the partner reports that its MMAs are done with that buffer.
+    // When the partner's half has arrived in ours, each thread adds its own half of its
+    // row in place, and the sum goes into dQacc by TMA bulk reductions: every dQ element
+    // crosses L2 once per pair instead of once per key block.  The stage buffer (its MMAs
+    // are done; the producer refills it only for the iteration after next, once the
+    // drain releases it) holds 128-row x 32-column fp32 boxes with 128-byte swizzle.
     const int row = (warp & 3) * 32 + lane;          // query row within the tile
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
+    const uint32_t peer = rank ^ 1u;
+    constexpr int HB = D / 64;                       // 32-column boxes per half
     bool ok = true;
     int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
@@ -518,45 +541,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int i = 0; i < D; ++i) asm volatile("" : "+f"(v[i])::"memory");
       tc_fence_before();
       mbar_arrive(BAR(W_DQFREE));
-      int* sem = a.deterministic ? a.sem + (size_t)bh * a.nq + m : nullptr;
-      if (a.deterministic) {
-        // Contributions to this query tile are added in key-block order 0, 1, 2, ...
-        if (leader) {
-          const unsigned long long t0 = globaltimer_ns();
-          while (ld_acquire(sem) != n) {
-            if (*abort_flag) break;
-            if (globaltimer_ns() - t0 > a.wait_ns) {
-              *abort_flag = 1;
-              atomicExch(a.status, DEV_TIMEOUT);
-              break;
-            }
+      int nbox, col0;
+      if (paired) {
+        // Our stage buffer may now receive the partner's half.
+        if (leader) mbar_arrive_cluster(mapa_shared(BAR(X_READY + st), peer));
+        const bool rdy = mbar_wait_cluster(BAR(X_READY + st), (it >> 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, rdy)) { ok = false; break; }
+        const uint32_t dst = mapa_shared(smem_u32(stage), peer);
+#pragma unroll
+        for (int j = 0; j < HB; ++j)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int i0 = j * 32 + 4 * c;            // column within a half
+            const float s0 = rank ? v[i0] : v[D / 2 + i0], s1 = rank ? v[i0 + 1] : v[D / 2 + i0 + 1];
+            const float s2 = rank ? v[i0 + 2] : v[D / 2 + i0 + 2], s3 = rank ? v[i0 + 3] : v[D / 2 + i0 + 3];
+            st_cluster_f4(dst + j * 16384 + row * 128 + ((c ^ (row & 7)) << 4), s0, s1, s2, s3);
           }
+        mbar_arrive_cluster(mapa_shared(BAR(X_RECV + st), peer));
+        const bool got = mbar_wait_cluster(BAR(X_RECV + st), (it >> 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+#pragma unroll
+        for (int j = 0; j < HB; ++j)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int i0 = j * 32 + 4 * c;
+            float4* cell = reinterpret_cast<float4*>(stage + j * 16384 + row * 128 + ((c ^ (row & 7)) << 4));
+            float4 x = *cell;
+            x.x += rank ? v[D / 2 + i0] : v[i0];
+            x.y += rank ? v[D / 2 + i0 + 1] : v[i0 + 1];
+            x.z += rank ? v[D / 2 + i0 + 2] : v[i0 + 2];
+            x.w += rank ? v[D / 2 + i0 + 3] : v[i0 + 3];
+            *cell = x;
+          }
+        nbox = HB;
+        col0 = int(rank) * (D / 2);
+      } else {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) {
+          const float* src = &v[bx * 32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
+                make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
         }
-        if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
-      }
-#pragma unroll
-      for (int bx = 0; bx < D / 32; ++bx) {
-        const float* src = &v[bx * 32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
-              make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
+        nbox = D / 32;
+        col0 = 0;
       }
       fence_proxy_async_smem();
       if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
       if (leader) {
-#pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + bx * 16384), bx * 32, m * 128, bh);
-        tma_store_commit();
+        // Deterministic: the pairs add into each (query tile, half) in pair order 0, 1, 2, ...
+        int* sem = a.deterministic ? a.sem + ((size_t)bh * a.nq + m) * 2 : nullptr;
+        const int h_lo = paired ? int(rank) : 0, h_hi = paired ? int(rank) : 1;
+        bool lok = true;   // leader only: a failure here stops the others at their next wait
         if (a.deterministic) {
-          tma_store_wait_all();                       // the adds have landed
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          __threadfence();
-          atomicAdd(sem, 1);
-        } else {
-          tma_store_wait_read();                      // the stage buffer has been read
+          const unsigned long long t0 = globaltimer_ns();
+          for (int hh = h_lo; hh <= h_hi && lok; ++hh)
+            while (ld_acquire(sem + hh) != pair) {
+              if (*abort_flag) { lok = false; break; }
+              if (globaltimer_ns() - t0 > a.wait_ns) {
+                *abort_flag = 1;
+                atomicExch(a.status, DEV_TIMEOUT);
+                lok = false;
+                break;
+              }
+            }
         }
-        mbar_arrive(BAR(W_EMPTY + st));
+        if (lok) {
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + bx * 16384), col0 + bx * 32, m * 128, bh);
+          tma_store_commit();
+          if (a.deterministic) {
+            tma_store_wait_all();                       // the adds have landed
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __threadfence();
+            for (int hh = h_lo; hh <= h_hi; ++hh) atomicAdd(sem + hh, 1);
+          } else {
+            tma_store_wait_read();                      // the stage buffer has been read
+          }
+          mbar_arrive(BAR(W_EMPTY + st));
+        }
       }
     }
     if (leader) {
@@ -566,7 +630,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // Neither CTA leaves while the other may still store into its shared memory or
+  // arrive on its barriers.
+  cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -579,7 +646,7 @@ template <int D>
 static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) {
   const long long rows = (long long)p.B * p.Hq * p.N;
   const int nq = (p.N + 127) / 128;
-  const int n_sem = p.deterministic ? p.B * p.Hq * nq : 0;
+  const int n_sem = p.deterministic ? p.B * p.Hq * nq * 2 : 0;
   {
     const long long blocks = std::max((rows + 15) / 16, ((long long)n_sem + 255) / 256);
     bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
@@ -601,12 +668,13 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     });
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     BwdKernelArgs a{};
-    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nq;
+    const int nkb = nq + (nq & 1);   // clusters of two CTAs: pad to an even count
+    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nkb;
     a.causal = p.causal; a.deterministic = p.deterministic;
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
-    const long long grid = (long long)p.B * p.Hkv * nq;
+    const long long grid = (long long)p.B * p.Hkv * nkb;
     kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dqacc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
