@@ -112,21 +112,6 @@ int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, co
   return ATTN_OK;
 }
 
-// [BH, rows, d] fp32 tensor, boxes of 128 rows x 32 columns (128 bytes), 128-byte swizzle.
-int make_map_f32(CUtensorMap* m, const void* base, int d, int rows, long long bh, const char* name) {
-  EncodeFn enc = get_encode();
-  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(g_encode_err));
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)rows * (cuuint64_t)d * 4};
-  cuuint32_t box[3] = {32, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "tensor map for %s: CUresult %d", name, (int)r);
-  return ATTN_OK;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
@@ -314,7 +299,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
   p.dq = dq; p.dk = dk; p.dv = dv;
   bwd_workspace_carve(workspace, B, Hq, Hkv, N, d, deterministic, &p);
-  if ((rc = make_map_f32(&maps.dqacc, p.dq_acc, d, N, (long long)B * Hq, "dq accumulator")) != ATTN_OK) return rc;
   p.wait_ns = (unsigned long long)g_wait_ns.load();
   p.status = s->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -3,6 +3,8 @@
 // Stages ("Hotelren FA4 summary" section 4.2, the five-stage backward pipeline; the
 // reverse-engineering page: P is recomputed, never stored):
 //   preprocess  D_i = sum_d dO_id O_id, LSE2_i = LSE_i * log2(e), dQacc = 0, counters = 0
+//               (dQacc rows are padded to whole 128-query tiles per head; the padding
+//               rows take the zero dQ of the queries past N and are never read)
 //   main        per CTA one key block of one K/V head, looping over the query tiles of
 //               every query head of the group:
 //                 S^T  = K Q^T                 (tcgen05, TMEM)
@@ -11,12 +13,12 @@
 //                 dV  += P^T dO                (A = P^T from TMEM)
 //                 dS^T = P^T o (dP^T - D)      (bf16, to shared memory)
 //                 dK  += dS^T Q                (A = dS^T, K-major view of the tile)
-//                 dQ   = dS K                  (A = dS, MN-major view of the same tile)
-//                 dQacc += dQ                  (CTA pairs on adjacent key blocks swap dQ
-//                                               halves through distributed shared memory;
-//                                               each adds the pair's sum for its half with
-//                                               fp32 TMA bulk reductions, in pair order when
-//                                               deterministic)
+//                 dQ^T = K^T dS^T              (both operands MN-major views of the K and
+//                                               dS^T tiles: TMEM lane i holds column i of dQ)
+//                 dQacc += dQ                  (fp32 red.global.add straight from TMEM
+//                                               registers, one 128-byte line of a dQacc row
+//                                               per warp instruction; in key-block order
+//                                               when deterministic)
 //               The transposed orientation (keys on TMEM lanes) makes every result land in
 //               the layout its consumer reads ("FlashAttention-4 explained" section 05).
 //   convert     dq = bf16(scale * dQacc)
@@ -24,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -36,8 +39,8 @@ size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int determinist
   (void)Hkv;
   const size_t rows = (size_t)B * Hq * N;
   const size_t nq = (size_t)B * Hq * ((N + 127) / 128);
-  size_t n = align256(rows * d * 4) + 2 * align256(rows * 4);
-  if (deterministic) n += align256(nq * 2 * 4);   // one counter per (query tile, dQ half)
+  size_t n = align256(nq * 128 * d * 4) + 2 * align256(rows * 4);
+  if (deterministic) n += align256(nq * 4);
   return n;
 }
 
@@ -45,8 +48,9 @@ void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int det
   (void)Hkv;
   char* b = static_cast<char*>(ws);
   const size_t rows = (size_t)B * Hq * N;
+  const size_t nq = (size_t)B * Hq * ((N + 127) / 128);
   p->dq_acc = reinterpret_cast<float*>(b);
-  b += align256(rows * d * 4);
+  b += align256(nq * 128 * d * 4);
   p->delta = reinterpret_cast<float*>(b);
   b += align256(rows * 4);
   p->lse2 = reinterpret_cast<float*>(b);
@@ -66,7 +70,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
                                                               const uint16_t* __restrict__ dout,
                                                               const float* __restrict__ lse, float* __restrict__ delta,
                                                               float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                              int* __restrict__ sem, long long rows, int n_sem) {
+                                                              int* __restrict__ sem, long long rows, int N, int npad,
+                                                              int n_sem) {
   constexpr int PER = D / 16;  // elements per thread
   const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
   const int sub = threadIdx.x & 15;
@@ -97,7 +102,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
-  float4* z = reinterpret_cast<float4*>(dq_acc + row * D + sub * PER);
+  const long long bh = row / N, r = row - bh * N;
+  float4* z = reinterpret_cast<float4*>(dq_acc + (bh * npad + r) * D + sub * PER);
 #pragma unroll
   for (int i = 0; i < PER / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (sub == 0) {
@@ -107,13 +113,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 }
 
 // ------------------------------------------------------------------------------------
-// Convert: dq = bf16(scale * dQacc), 8 elements per thread.
+// Convert: dq = bf16(scale * dQacc), 8 elements per thread (dQacc rows padded per head).
 // ------------------------------------------------------------------------------------
+template <int D>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                           float scale, long long n8) {
+                                                           float scale, long long n8, int N, int npad) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    const long long row = i / (D / 8), bh = row / N;
+    const long long src = ((bh * npad + (row - bh * N)) * D) / 8 + i % (D / 8);
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * src];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * src + 1];
     uint4 r;
     r.x = pack_bf16x2(a.x * scale, a.y * scale);
     r.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -128,8 +137,8 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 // Main backward kernel.
 // Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle,
 //        4-7 and 8-11 "compute" (P^T, dS^T; keys on TMEM lanes; queries 0-63 and 64-127),
-//        12-15 "drain" (dQ rows -> dQacc).
-// TMEM columns: S^T/P^T [0,128), dP^T then dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+//        12-15 "drain" (dQ^T -> dQacc).
+// TMEM columns: S^T/P^T [0,128), dP^T then dQ^T [128,256), dV [256,256+D), dK [256+D,256+2D).
 // ------------------------------------------------------------------------------------
 constexpr int kBwdThreads = 512;
 
@@ -148,17 +157,18 @@ struct BwdCfg {
   static constexpr uint32_t SMEM = 1024 + OFF_CTRL + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KB = idesc_bf16_f32(128, D, false, true);     // dV, dK
-  static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
+  // dQ^T: M = 128 rows of K^T (for D = 64 the upper 64 read the V tile that follows K in
+  // shared memory: padding that the drain ignores), N = 128 queries.
+  static constexpr uint32_t IDESC_DQT = idesc_bf16_f32(128, 128, true, true);
 };
 
 enum {
   W_KV = 0, W_FULL = 1 /* +stage */, W_EMPTY = 3 /* +stage */, W_S = 5, W_DP = 6, W_P = 7, W_DS = 8, W_DQ = 9,
-  W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13, W_GC = 14, W_GD = 15,
-  W_DRAINED = 16, // the drain warpgroup has finished (one arrival)
-  W_GC1 = 17,     // staging sync of the second compute warpgroup
-  X_READY = 18,   // +stage: the partner CTA's stage buffer may receive our dQ half (1 remote arrival)
-  X_RECV = 20,    // +stage: the partner's dQ half has landed in our stage buffer (128 remote arrivals)
-  W_COUNT = 22
+  W_DQFREE = 10, W_DSFREE = 11, W_DONE = 12, W_EPI = 13,
+  W_VFULL = 14,   // -LSE2 and -D of the next tile are in shared memory (32 arrivals, warp 3)
+  W_GD = 15,
+  W_VFREE = 16,   // both compute warpgroups are done with those vectors (256 arrivals)
+  W_COUNT = 17
 };
 
 // Bounded barrier for one warpgroup (128 threads) built on an mbarrier: every thread
@@ -182,9 +192,15 @@ __device__ __forceinline__ void reg_fence_b(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+// Adds x at base + OFF bytes: one instruction with an immediate offset.
+template <int OFF>
+__device__ __forceinline__ void red_add_f32_at(float* base, float x) {
+  asm volatile("red.global.add.f32 [%0+%1], %2;" ::"l"(base), "n"(OFF), "f"(x) : "memory");
+}
+// dQacc rows 0..127 of a tile (row stride D floats), column = this lane.
+template <int D, int... J>
+__device__ __forceinline__ void red_add_rows(float* base, const float (&v)[128], std::integer_sequence<int, J...>) {
+  (red_add_f32_at<J * D * 4>(base, v[J]), ...);
 }
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -193,7 +209,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 }
 
 struct BwdKernelArgs {
-  int B, Hq, Hkv, N, g, nq, nkb /* key blocks per head rounded up to even */, causal, deterministic;
+  int B, Hq, Hkv, N, g, nq, nkb, causal, deterministic;
   float c, scale;
   const float* lse2;
   const float* delta;
@@ -204,11 +220,11 @@ struct BwdKernelArgs {
 };
 
 template <int D>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                    const __grid_constant__ CUtensorMap tm_dqacc, const BwdKernelArgs a) {
+                    const BwdKernelArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,27 +238,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   float* vec_d = vec_lse + 128;
 
   const int warp = warp_id(), lane = lane_id();
-  // The two CTAs of a cluster take adjacent key blocks n = 2p, 2p + 1 of one K/V head
-  // and visit the same query tiles in the same order.  When the head has an odd number
-  // of key blocks the last cluster's second CTA has no block ("dead"): it only joins the
-  // cluster barriers, and its partner adds its whole dQ by itself ("unpaired").
   const int bkv = blockIdx.x / a.nkb, n = blockIdx.x % a.nkb;
   const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
-  const uint32_t rank = cluster_ctarank();            // == n & 1
-  const int pair = n >> 1;
-  const bool live = n < a.nq;
-  const bool paired = (n | 1) < a.nq;
-  const int m0 = a.causal ? 2 * pair : 0;
+  const int m0 = a.causal ? n : 0;
   const int n_m = a.nq - m0;
-  const int n_iter = live ? a.g * n_m : 0;
+  const int n_iter = a.g * n_m;
   WaitCtl wc{a.wait_ns, a.status, abort_flag};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
-      mbar_init(BAR(i), (i == W_P || i == W_DS) ? 256
-                        : (i == W_DQFREE || i == W_EPI || i == W_GC || i == W_GC1 || i == W_GD || i == X_RECV ||
-                           i == X_RECV + 1) ? 128 : 1);
-    // W_EMPTY: released by the drain's leader (one arrival), W_DRAINED: one arrival.
+      mbar_init(BAR(i), (i == W_P || i == W_DS || i == W_VFREE) ? 256
+                        : (i == W_DQFREE || i == W_EPI || i == W_GD) ? 128 : (i == W_VFULL) ? 32 : 1);
+    // W_EMPTY: released by a commit once the stage's last MMA (dK) has finished.
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -251,30 +258,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' barriers exist before either arrives on the other's
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
 
-  // Query tiles are visited in a staggered order: pair p starts at query tile p, so the
-  // pairs of one head add into different dQ rows at any moment (they would otherwise
-  // all hit the same rows together).  Causal pairs start at the diagonal tile of their
-  // first key block (for the second block that tile is fully masked).  In deterministic
-  // mode each pair still trails its predecessor by about one iteration.
+  // Query tiles are visited in a staggered order: key block n starts at query tile n, so
+  // the CTAs of one head add into different dQ rows at any moment (they would otherwise
+  // all hit the same rows together).  Causal CTAs already start at their diagonal tile.
+  // In deterministic mode each CTA still trails its predecessor by about one iteration.
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
-    m = a.causal ? m0 + it % n_m : (it % n_m + pair) % n_m;
+    m = a.causal ? m0 + it % n_m : (it % n_m + n) % n_m;
     bh = b * a.Hq + hkv * a.g + r;
   };
 
-  // Register split (per thread): warpgroup 0 (producer, MMA) 56, two compute warpgroups
-  // 152 each, drain 152: 56 + 3 x 152 = 512 = 4 x 128, the launch's 128 x 512 threads.  Each
-  // role's code sits inside its own branch so that its limit covers it.
+  // Register split (per thread): warpgroup 0 (producer, MMA) 88, the two compute
+  // warpgroups 136 each, drain 152: 88 + 2 x 136 + 152 = 512 = 4 x 128, the launch's
+  // 128 x 512 threads, and no role spills.  Each role's code sits inside its own branch
+  // so that its limit covers it.
   const int wg = warp >> 2;
-  if (!live) {
-    // no key block: nothing to compute
-  } else if (wg == 0) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  if (wg == 0) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
@@ -315,19 +320,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       bool ok = mbar_wait(BAR(W_KV), 0, wc);
       tc_fence_after();
       const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V, dsb = sbase + C::OFF_DS;
-      for (int it = 0; it < n_iter && ok; ++it) {
+      // S^T = K Q^T for tile `it`, once its Q/dO stage has landed.
+      auto issue_s = [&](int it) -> bool {
         const int st = it & 1;
-        if (!mbar_wait(BAR(W_FULL + st), (it >> 1) & 1, wc)) { ok = false; break; }
+        if (!mbar_wait(BAR(W_FULL + st), (it >> 1) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t qs = sbase + C::OFF_STAGE + st * 2 * C::TILE, dos = qs + C::TILE;
-        // S^T = K Q^T
+        const uint32_t qs = sbase + C::OFF_STAGE + st * 2 * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
           mma_ss(tS, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024), C::IDESC_S, kk > 0);
         }
         mma_commit(BAR(W_S));
-        // dP^T = V dO^T, once the previous dQ has left those columns
+        return true;
+      };
+      if (ok && n_iter > 0) ok = issue_s(0);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int st = it & 1;
+        const uint32_t qs = sbase + C::OFF_STAGE + st * 2 * C::TILE, dos = qs + C::TILE;
+        // dP^T = V dO^T, once the previous dQ^T has left those columns
         if (it > 0 && !mbar_wait(BAR(W_DQFREE), (it - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -343,7 +354,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dos + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
                  (it > 0 || kk > 0));
-        // dK += dS^T Q ; dQ = dS K
+        // The next tile's S^T goes ahead of this tile's dK and dQ, so that its
+        // probabilities are computed while they run.  MMAs of one thread execute in issue
+        // order: S^T lands in the columns of P^T only after dV has read them.
+        if (it + 1 < n_iter && !issue_s(it + 1)) { ok = false; break; }
+        // dK += dS^T Q ; dQ^T = K^T dS^T
         if (!mbar_wait(BAR(W_DS), it & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -352,11 +367,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           mma_ss(tdK, sdesc_sw128(dsb + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
                  (it > 0 || kk > 0));
         }
+        mma_commit(BAR(W_EMPTY + st));  // dK was the stage's last reader: the producer may refill it
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tdP, sdesc_sw128(dsb + kk * 2048, C::CHUNK, 1024), sdesc_sw128(kb + kk * 2048, C::CHUNK, 1024),
-                 C::IDESC_DQ, kk > 0);
-        mma_commit(BAR(W_DQ));          // the drain releases this Q/dO stage after staging dQ in it
+          mma_ss(tdP, sdesc_sw128(kb + kk * 2048, C::CHUNK, 1024), sdesc_sw128(dsb + kk * 2048, C::CHUNK, 1024),
+                 C::IDESC_DQT, kk > 0);
+        mma_commit(BAR(W_DQ));
         mma_commit(BAR(W_DSFREE));
       }
       mma_commit(BAR(W_DONE));
@@ -364,9 +380,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       while (!mbar_try_wait(BAR(W_DONE), 0) && globaltimer_ns() - t0 < a.wait_ns) {
       }
     }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ vector loader
+    // -LSE2 and -D of each tile's 128 queries (lane + 32u), fetched into registers one
+    // tile ahead so that their global-memory latency hides behind the current tile, and
+    // written to shared memory once both compute warpgroups are done with the previous
+    // ones.  Queries past N get -inf / 0, which makes their probabilities and dS zero.
+    float nl[4], nd[4];
+    auto fetch = [&](int it) {
+      int bh, m;
+      iter_head_row(it, bh, m);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int qj = m * 128 + u * 32 + lane;
+        nl[u] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
+        nd[u] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
+      }
+    };
+    if (n_iter > 0) fetch(0);
+    for (int it = 0; it < n_iter; ++it) {
+      if (it > 0 && !warp_wait_b(BAR(W_VFREE), (it - 1) & 1, wc)) break;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        vec_lse[u * 32 + lane] = nl[u];
+        vec_d[u * 32 + lane] = nd[u];
+      }
+      mbar_arrive(BAR(W_VFULL));
+      if (it + 1 < n_iter) fetch(it + 1);
+    }
   }
   } else if (wg == 1 || wg == 2) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 136;");
     // ------------------------------------------------------------------ compute: P^T, dS^T
     // Two warpgroups share the work column-wise: half h owns queries [64h, 64h + 64) of
     // every key row.  Its packed P goes to TMEM columns [64h, 64h + 32), inside its own
@@ -377,20 +421,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + C::OFF_DS;
     bool ok = true;
-    int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
       int bh, m;
       iter_head_row(it, bh, m);
-      // Stage this half's -LSE2 and -D (index = query within the tile); the first sync keeps
-      // the previous tile's readers ahead of the overwrite.  Queries past N get -inf / 0,
-      // which makes their probabilities and dS exactly zero.
-      if (!group_sync(BAR(h ? W_GC1 : W_GC), gphase, wc)) { ok = false; break; }
-      if (row < 64) {
-        const int qc = h * 64 + row, qj = m * 128 + qc;
-        vec_lse[qc] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
-        vec_d[qc] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
-      }
-      if (!group_sync(BAR(h ? W_GC1 : W_GC), gphase, wc)) { ok = false; break; }
+      // This tile's -LSE2 and -D (index = query within the tile), from the vector loader.
+      if (!warp_wait_b(BAR(W_VFULL), it & 1, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_S), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
       // Visible queries for this key row: qj >= kr when causal, qj < N, and the key itself < N.
@@ -466,10 +501,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(BAR(W_DS));
+      mbar_arrive(BAR(W_VFREE));
     }
     // Epilogue: dV and scale * dK -> bf16 -> stage 0 buffers -> TMA store, once every MMA
-    // has completed and the drain no longer stages dQ in the stage buffers.
-    if (h == 0 && ok && warp_wait_b(BAR(W_DONE), 0, wc) && warp_wait_b(BAR(W_DRAINED), 0, wc)) {
+    // has completed (the last loads into the stage buffers have then been consumed).
+    if (h == 0 && ok && warp_wait_b(BAR(W_DONE), 0, wc)) {
       tc_fence_after();
       uint8_t* sv = smem + C::OFF_STAGE;
       uint8_t* sk = sv + C::TILE;
@@ -510,130 +546,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
     // ------------------------------------------------------------------ drain: dQ -> dQacc
-    // dQ leaves TMEM into registers (the columns are then free for the next dP).  A paired
-    // CTA keeps dQ columns [rank * D/2, rank * D/2 + D/2) and stores the other half of
-    // each row straight into its partner's stage buffer for this iteration (distributed
-    // shared memory), once the partner reports that its MMAs are done with that buffer.
-    // When the partner's half has arrived in ours, each thread adds its own half of its
-    // row in place, and the sum goes into dQacc by TMA bulk reductions: every dQ element
-    // crosses L2 once per pair instead of once per key block.  The stage buffer (its MMAs
-    // are done; the producer refills it only for the iteration after next, once the
-    // drain releases it) holds 128-row x 32-column fp32 boxes with 128-byte swizzle.
-    const int row = (warp & 3) * 32 + lane;          // query row within the tile
+    // dQ is formed transposed, so TMEM lane i holds column i of dQ for the tile's 128
+    // queries.  Lane i of a warp adds element i of one query row: each red.global.add of a
+    // warp covers 32 consecutive floats (one 128-byte line) of a dQacc row.  The drain
+    // reads TMEM and writes L2 only; it never touches shared memory, which the MMAs need.
+    const int dcol = (warp & 3) * 32 + lane;         // dQ column = TMEM lane
+    const bool has_col = (warp & 3) * 32 < D;        // D = 64: lanes 64-127 hold padding
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
-    const uint32_t peer = rank ^ 1u;
-    constexpr int HB = D / 64;                       // 32-column boxes per half
     bool ok = true;
     int gphase = 0;
     for (int it = 0; it < n_iter && ok; ++it) {
       int bh, m;
       iter_head_row(it, bh, m);
-      const int st = it & 1;
-      uint8_t* stage = smem + C::OFF_STAGE + st * 2 * C::TILE;
       if (!warp_wait_b(BAR(W_DQ), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
-      float v[D];
+      float v[128];
+      if (has_col) {
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) tmem_ld32(tdP + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[q * 32]));
-      tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) tmem_ld32(tdP + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[q * 32]));
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < D; ++i) asm volatile("" : "+f"(v[i])::"memory");
+        for (int i = 0; i < 128; ++i) asm volatile("" : "+f"(v[i])::"memory");
+      }
       tc_fence_before();
       mbar_arrive(BAR(W_DQFREE));
-      int nbox, col0;
-      if (paired) {
-        // Our stage buffer may now receive the partner's half.
-        if (leader) mbar_arrive_cluster(mapa_shared(BAR(X_READY + st), peer));
-        const bool rdy = mbar_wait_cluster(BAR(X_READY + st), (it >> 1) & 1, wc);
-        if (!__all_sync(0xffffffffu, rdy)) { ok = false; break; }
-        const uint32_t dst = mapa_shared(smem_u32(stage), peer);
-#pragma unroll
-        for (int j = 0; j < HB; ++j)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int i0 = j * 32 + 4 * c;            // column within a half
-            const float s0 = rank ? v[i0] : v[D / 2 + i0], s1 = rank ? v[i0 + 1] : v[D / 2 + i0 + 1];
-            const float s2 = rank ? v[i0 + 2] : v[D / 2 + i0 + 2], s3 = rank ? v[i0 + 3] : v[D / 2 + i0 + 3];
-            st_cluster_f4(dst + j * 16384 + row * 128 + ((c ^ (row & 7)) << 4), s0, s1, s2, s3);
-          }
-        mbar_arrive_cluster(mapa_shared(BAR(X_RECV + st), peer));
-        const bool got = mbar_wait_cluster(BAR(X_RECV + st), (it >> 1) & 1, wc);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-#pragma unroll
-        for (int j = 0; j < HB; ++j)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int i0 = j * 32 + 4 * c;
-            float4* cell = reinterpret_cast<float4*>(stage + j * 16384 + row * 128 + ((c ^ (row & 7)) << 4));
-            float4 x = *cell;
-            x.x += rank ? v[D / 2 + i0] : v[i0];
-            x.y += rank ? v[D / 2 + i0 + 1] : v[i0 + 1];
-            x.z += rank ? v[D / 2 + i0 + 2] : v[i0 + 2];
-            x.w += rank ? v[D / 2 + i0 + 3] : v[i0 + 3];
-            *cell = x;
-          }
-        nbox = HB;
-        col0 = int(rank) * (D / 2);
-      } else {
-#pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) {
-          const float* src = &v[bx * 32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(stage + bx * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) =
-                make_float4(src[4 * c], src[4 * c + 1], src[4 * c + 2], src[4 * c + 3]);
-        }
-        nbox = D / 32;
-        col0 = 0;
-      }
-      fence_proxy_async_smem();
-      if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
-      if (leader) {
-        // Deterministic: the pairs add into each (query tile, half) in pair order 0, 1, 2, ...
-        int* sem = a.deterministic ? a.sem + ((size_t)bh * a.nq + m) * 2 : nullptr;
-        const int h_lo = paired ? int(rank) : 0, h_hi = paired ? int(rank) : 1;
-        bool lok = true;   // leader only: a failure here stops the others at their next wait
-        if (a.deterministic) {
+      int* sem = a.deterministic ? a.sem + (size_t)bh * a.nq + m : nullptr;
+      if (a.deterministic) {
+        // Contributions to this query tile are added in key-block order 0, 1, 2, ...
+        if (leader) {
           const unsigned long long t0 = globaltimer_ns();
-          for (int hh = h_lo; hh <= h_hi && lok; ++hh)
-            while (ld_acquire(sem + hh) != pair) {
-              if (*abort_flag) { lok = false; break; }
-              if (globaltimer_ns() - t0 > a.wait_ns) {
-                *abort_flag = 1;
-                atomicExch(a.status, DEV_TIMEOUT);
-                lok = false;
-                break;
-              }
+          while (ld_acquire(sem) != n) {
+            if (*abort_flag) break;
+            if (globaltimer_ns() - t0 > a.wait_ns) {
+              *abort_flag = 1;
+              atomicExch(a.status, DEV_TIMEOUT);
+              break;
             }
-        }
-        if (lok) {
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_reduce_add_3d(&tm_dqacc, smem_u32(stage + bx * 16384), col0 + bx * 32, m * 128, bh);
-          tma_store_commit();
-          if (a.deterministic) {
-            tma_store_wait_all();                       // the adds have landed
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __threadfence();
-            for (int hh = h_lo; hh <= h_hi; ++hh) atomicAdd(sem + hh, 1);
-          } else {
-            tma_store_wait_read();                      // the stage buffer has been read
           }
-          mbar_arrive(BAR(W_EMPTY + st));
+        }
+        if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
+      }
+      if (has_col) {
+        // Rows are padded to whole tiles, so queries past N add into padding rows.
+        float* dst = a.dq_acc + ((size_t)bh * a.nq * 128 + (size_t)m * 128) * D + dcol;
+        red_add_rows<D>(dst, v, std::make_integer_sequence<int, 128>{});
+      }
+      if (a.deterministic) {
+        __threadfence();                              // this thread's adds are performed
+        if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
+        if (leader) {
+          __threadfence();
+          atomicAdd(sem, 1);
         }
       }
-    }
-    if (leader) {
-      tma_store_wait_all();
-      mbar_arrive(BAR(W_DRAINED));
     }
   }
 
   tc_fence_before();
-  __syncwarp();
-  // Neither CTA leaves while the other may still store into its shared memory or
-  // arrive on its barriers.
-  cluster_sync_all();
+  __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -646,12 +617,12 @@ template <int D>
 static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) {
   const long long rows = (long long)p.B * p.Hq * p.N;
   const int nq = (p.N + 127) / 128;
-  const int n_sem = p.deterministic ? p.B * p.Hq * nq * 2 : 0;
+  const int n_sem = p.deterministic ? p.B * p.Hq * nq : 0;
   {
     const long long blocks = std::max((rows + 15) / 16, ((long long)n_sem + 255) / 256);
     bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
         static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.delta, p.lse2, p.dq_acc,
-        p.sem, rows, n_sem);
+        p.sem, rows, p.N, nq * 128, n_sem);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -668,14 +639,13 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     });
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     BwdKernelArgs a{};
-    const int nkb = nq + (nq & 1);   // clusters of two CTAs: pad to an even count
-    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nkb;
+    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nq;
     a.causal = p.causal; a.deterministic = p.deterministic;
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
-    const long long grid = (long long)p.B * p.Hkv * nkb;
-    kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dqacc, a);
+    const long long grid = (long long)p.B * p.Hkv * nq;
+    kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -685,7 +655,8 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long blocks = std::min<long long>((n8 + 255) / 256, (long long)sms * 8);
-    bwd_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, static_cast<uint16_t*>(p.dq), p.scale, n8);
+    bwd_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, static_cast<uint16_t*>(p.dq), p.scale, n8, p.N,
+                                                            nq * 128);
     return cudaGetLastError();
   }
 }

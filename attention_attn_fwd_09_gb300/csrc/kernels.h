@@ -46,7 +46,7 @@ struct BwdParams {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* dq_acc;             // [B, Hq, N, D] fp32 workspace
+  float* dq_acc;             // [B, Hq, ceil(N/128)*128, D] fp32 workspace (rows padded to whole tiles)
   float* delta;              // [B, Hq, N] fp32 workspace (rowsum(dO o O))
   float* lse2;               // [B, Hq, N] fp32 workspace (LSE * log2 e)
   int* sem;                  // deterministic-order counters
@@ -55,7 +55,6 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dout, dk, dv;
-  CUtensorMap dqacc;   // fp32 [B*Hq, N, d], boxes of 128 rows x 32 columns, 128-byte swizzle
 };
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic);
