@@ -238,7 +238,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* vec_d = vec_lse + 128;
 
   const int warp = warp_id(), lane = lane_id();
-  const int bkv = blockIdx.x / a.nkb, n = blockIdx.x % a.nkb;
+  // Causal: key block n has nq - n query tiles, so blocks are launched in order of n
+  // across all heads (longest first).  Otherwise the blocks of one head run together
+  // and share its Q and dO tiles in L2.
+  const int nbkv = a.B * a.Hkv;
+  const int bkv = a.causal ? blockIdx.x % nbkv : blockIdx.x / a.nkb;
+  const int n = a.causal ? blockIdx.x / nbkv : blockIdx.x % a.nkb;
   const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
   const int m0 = a.causal ? n : 0;
   const int n_m = a.nq - m0;
