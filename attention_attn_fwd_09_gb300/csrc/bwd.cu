@@ -271,10 +271,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Query tiles are visited in a staggered order: key block n starts at query tile n, so
   // the CTAs of one head add into different dQ rows at any moment (they would otherwise
   // all hit the same rows together).  Causal CTAs already start at their diagonal tile.
-  // In deterministic mode each CTA still trails its predecessor by about one iteration.
+  // Deterministic mode instead visits the tiles in one descending order shared by all key
+  // blocks of a head (causal blocks end at their diagonal), so block n reaches each tile
+  // in the same iteration as block n - 1 and waits only for that block's adds to land.
+  const int m_start = a.deterministic ? a.nq - 1 : n, m_step = a.deterministic ? -1 : 1;
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
-    m = a.causal ? m0 + it % n_m : (it % n_m + n) % n_m;
+    m = m_start + m_step * (it - r * n_m);
+    if (m >= a.nq) m -= a.nq;                        // non-causal rotation wraps around
     bh = b * a.Hq + hkv * a.g + r;
   };
 
