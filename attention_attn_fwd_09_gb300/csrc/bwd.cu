@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 
 // ------------------------------------------------------------------------------------
 // Main backward kernel.
-// Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle,
+// Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 -LSE2/-D prefetch,
 //        4-7 and 8-11 "compute" (P^T, dS^T; keys on TMEM lanes; queries 0-63 and 64-127),
 //        12-15 "drain" (dQ^T -> dQacc).
 // TMEM columns: S^T/P^T [0,128), dP^T then dQ^T [128,256), dV [256,256+D), dK [256+D,256+2D).
