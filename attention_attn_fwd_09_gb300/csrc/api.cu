@@ -1,6 +1,7 @@
 // C-ABI entry points (declared in include/attn.h): argument checks, TMA tensor maps,
 // kernel selection and launch.  No allocation on any call path; every launch goes on
 // the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -240,7 +241,19 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.status = s->status;
   p.rescale_count = g_count_rescales.load() ? s->rescale : nullptr;
   p.test_skip_first_kv = g_test_skip_kv.load();
-  const long long grid = (long long)p.n_rowslots * p.units_per_row;
+  // Units of two tiles, one CTA each.  When the last wave would hold few units (at most
+  // half the SMs) they are split into one-tile CTAs, so that the last wave takes one tile's
+  // time instead of two tiles' (non-causal only: causal units come longest first, so the
+  // last ones are short already).
+  const long long units = (long long)p.n_rowslots * p.units_per_row;
+  p.split_from = (int)std::min<long long>(units, 0x7fffffffLL);
+  if (!p.causal) {
+    const long long sms = std::max(1, s->sms);
+    const long long rem = units % sms;
+    if (units >= sms && rem > 0 && 2 * rem <= sms) p.split_from = (int)(units - rem);
+    else if (units < sms && 2 * units <= sms) p.split_from = 0;
+  }
+  const long long grid = p.split_from + 2 * (units - p.split_from);
   if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_fwd(maps, p, d, g_poly.load(), (int)grid, st);

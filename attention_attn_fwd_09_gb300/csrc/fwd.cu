@@ -165,7 +165,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int wg = warp >> 2;
-  const Tiles T = map_unit(p, blockIdx.x);
+  // CTAs past split_from each take one tile of a unit (the other half of the unit goes to
+  // the next CTA); the lone tile always sits in slot 0.
+  Tiles T;
+  if ((int)blockIdx.x < p.split_from) {
+    T = map_unit(p, blockIdx.x);
+  } else {
+    const int k = (int)blockIdx.x - p.split_from;
+    T = map_unit(p, p.split_from + k / 2);
+    if (k & 1) {
+      T.n[0] = T.n[1];
+      T.row0[0] = T.row0[1];
+      T.bh[0] = T.bh[1];
+    }
+    T.n[1] = 0;
+  }
   const int nmax = max(T.n[0], T.n[1]);
   WaitCtl wc{p.wait_ns, p.status, abort_flag};
 

@@ -15,6 +15,7 @@ struct FwdParams {
   int n_qblk, n_kvblk;     // ceil(N / 128)
   int units_per_row;       // CTAs per query-row slot (see fwd.cu unit mapping)
   int n_rowslots;          // query-row slots per head (pair) sequence
+  int split_from;          // units >= split_from run as two one-tile CTAs (the last, partial wave)
   float c;                 // scale * log2(e)
   float tau;               // conditional-rescale threshold, log2 units
   float* lse;              // [B, Hq, N] fp32, natural log
