@@ -39,7 +39,9 @@ def check(got, ref, what):
 
 
 SHAPES = [(1, 2, 2, 128, 64), (1, 2, 2, 200, 128), (1, 4, 2, 256, 128), (1, 4, 1, 300, 64), (2, 2, 2, 1, 128),
-          (1, 3, 1, 130, 128), (2, 2, 1, 512, 64)]
+          (1, 3, 1, 130, 128), (2, 2, 1, 512, 64),
+          # one row short of, one past, and one past two whole 128-row tiles
+          (1, 2, 2, 127, 128), (1, 2, 1, 129, 64), (1, 2, 2, 257, 128)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dHq%dHkv%dN%dd%d" % s)

@@ -55,6 +55,20 @@ def test_shapes_ragged_grouped(A, shape, causal):
     check_fwd(o, lse, O, L, f"{shape} causal={causal}")
 
 
+def test_last_wave_one_tile_ctas(A):
+    # 2 x 81 heads of N = 256 (two query tiles) are 162 two-tile units.  On GPUs with 132
+    # to 152 SMs the last wave holds 10 to 30 of them, which run as one-tile CTAs; the last
+    # heads are in that wave and the first ones are not.
+    B, H, N, d = 2, 81, 256, 128
+    x = make_inputs(55, B, H, H, N, d)
+    scale = default_scale(d)
+    o, lse = run(A, x, False, scale)
+    heads = [(0, 0), (1, 78), (1, 80)]
+    O, L = oracle.attn_fwd(x["q"], x["k"], x["v"], False, scale, heads=heads)
+    for s, (b, h) in enumerate(heads):
+        check_fwd(o[b, h], lse[b, h], O[s], L[s], f"b{b} h{h}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_train_workload_heads(A, causal):
     w = WORKLOADS["train2k"]
