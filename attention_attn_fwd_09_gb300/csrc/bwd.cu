@@ -223,6 +223,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 
 struct BwdKernelArgs {
   int B, Hq, Hkv, N, g, nq, nkb, causal, deterministic;
+  int det_rotate;   // deterministic with the rotating per-tile order (see the kernel)
   float c, scale;
   const float* lse2;
   const float* delta;
@@ -284,10 +285,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Query tiles are visited in a staggered order: key block n starts at query tile n, so
   // the CTAs of one head add into different dQ rows at any moment (they would otherwise
   // all hit the same rows together).  Causal CTAs already start at their diagonal tile.
-  // Deterministic mode instead visits the tiles in one descending order shared by all key
-  // blocks of a head (causal blocks end at their diagonal), so block n reaches each tile
-  // in the same iteration as block n - 1 and waits only for that block's adds to land.
-  const int m_start = a.deterministic ? a.nq - 1 : n, m_step = a.deterministic ? -1 : 1;
+  // Deterministic mode fixes, for every tile, the order in which key blocks add into it:
+  //  - rotating (non-causal, when every key block of a head fits on the GPU at once): the
+  //    staggered order above, with tile m taking blocks m, m - 1, m - 2, ... (mod nq) —
+  //    the order in which they reach it, each one iteration after the previous, so a
+  //    block waits only for an add made an iteration earlier.  A block waits on a block
+  //    with a higher index, so the whole head must be resident: the host enables it only
+  //    when a head's blocks take at most half the SMs.
+  //  - otherwise: one descending tile order shared by all key blocks of a head (causal
+  //    blocks end at their diagonal), tile m taking blocks 0, 1, 2, ...; block n reaches
+  //    each tile in the same iteration as block n - 1 and waits for that block's adds.
+  const bool shared_order = a.deterministic && !a.det_rotate;
+  const int m_start = shared_order ? a.nq - 1 : n, m_step = shared_order ? -1 : 1;
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
     m = m_start + m_step * (it - r * n_m);
@@ -595,10 +604,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(BAR(W_DQFREE));
       int* sem = a.deterministic ? a.sem + (size_t)bh * a.nq + m : nullptr;
       if (a.deterministic) {
-        // Contributions to this query tile are added in key-block order 0, 1, 2, ...
+        // This block's turn among the tile's contributions (see the tile order above).
+        const int turn = a.det_rotate ? it - (it / n_m) * n_m : n;
         if (leader) {
           const unsigned long long t0 = globaltimer_ns();
-          while (ld_acquire(sem) != n) {
+          while (ld_acquire(sem) != turn) {
             if (*abort_flag) break;
             if (globaltimer_ns() - t0 > a.wait_ns) {
               *abort_flag = 1;
@@ -663,6 +673,11 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     BwdKernelArgs a{};
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nq;
     a.causal = p.causal; a.deterministic = p.deterministic;
+    {
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      a.det_rotate = (p.deterministic && !p.causal && 2 * nq <= sms) ? 1 : 0;
+    }
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
