@@ -4,7 +4,8 @@ Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 import this package.  The product path (the CUDA library and its Python binding) never
 imports it, and this package imports nothing from the product path.
 
-``attn_fwd`` / ``attn_bwd`` wrap the plain-C fp64 implementation in ``attn_oracle.c``
+``attn_fwd`` / ``attn_bwd`` (and ``attn_fwd_kv``, queries after a longer key cache) wrap
+the plain-C fp64 implementation in ``attn_oracle.c``
 (materialised S and P, chain-rule gradients); ``tiled`` holds a step-by-step fp32
 emulation of the tiled online softmax with the conditional rescale.
 """
@@ -44,6 +45,8 @@ def _load():
             lib.oracle_attn_fwd.restype = i
             lib.oracle_attn_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, dbl, i, p, p, p, p]
             lib.oracle_attn_bwd.restype = i
+            lib.oracle_attn_fwd_kv.argtypes = [p, p, p, i, i, i, i, i, i, i, dbl, i, p, p, p]
+            lib.oracle_attn_fwd_kv.restype = i
             _lib = lib
     return _lib
 
@@ -111,3 +114,25 @@ def attn_bwd(q, k, v, do, causal: bool, scale: float, kv_heads=None):
     if kv_heads is None:
         return dQ.reshape(B, Hq, N, d), dK.reshape(B, Hkv, N, d), dV.reshape(B, Hkv, N, d)
     return dQ, dK, dV
+
+
+def attn_fwd_kv(q, k, v, causal: bool, scale: float, heads=None):
+    """fp64 forward with Nq queries after Nk >= Nq keys: ``q [B,Hq,Nq,d]``, ``k``/``v
+    [B,Hkv,Nk,d]`` in bf16.  Causal: query i sees keys j <= i + Nk - Nq.  Returns (O, LSE)
+    shaped like ``attn_fwd``'s with Nq rows."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, Hq, Nq, d = qb.shape
+    Hkv, Nk = kb.shape[1], kb.shape[2]
+    if heads is None:
+        sel = np.arange(B * Hq, dtype=np.int32)
+    else:
+        sel = np.asarray([b * Hq + h for b, h in heads], dtype=np.int32)
+    O = np.zeros((len(sel), Nq, d), dtype=np.float64)
+    L = np.zeros((len(sel), Nq), dtype=np.float64)
+    rc = _load().oracle_attn_fwd_kv(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                                    float(scale), len(sel), _ptr(sel), _ptr(O), _ptr(L))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_kv failed ({rc})")
+    if heads is None:
+        return O.reshape(B, Hq, Nq, d), L.reshape(B, Hq, Nq)
+    return O, L

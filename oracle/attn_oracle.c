@@ -213,3 +213,70 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   free(Qd); free(Kd); free(Vd); free(dOd); free(P); free(dS);
   return rc;
 }
+
+/*
+ * Forward with a key/value sequence longer than the query sequence (queries appended
+ * after a cache of keys): q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d].  Query i stands at position
+ * i + (Nk - Nq) of the key sequence, so with causal it sees keys j <= i + Nk - Nq
+ * (the mask aligned at the bottom-right corner; Nq = Nk is the square case above).
+ * Causal needs Nq <= Nk (every query sees at least one key).  sel[s] = b * Hq + hq;
+ * outputs O[s, Nq, d] and LSE[s, Nq].  Returns 0, -1 on bad arguments, -2 without memory.
+ */
+int oracle_attn_fwd_kv(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int Hq, int Hkv, int Nq,
+                       int Nk, int d, int causal, double scale, int nsel, const int* sel, double* O, double* LSE) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || Hq % Hkv != 0) return -1;
+  if (causal && Nq > Nk) return -1;
+  const int g = Hq / Hkv;
+  const int off = Nk - Nq;
+  const size_t qd = (size_t)Nq * d, kd = (size_t)Nk * d;
+  double* Qd = (double*)malloc(qd * sizeof(double) + 1);
+  double* Kd = (double*)malloc(kd * sizeof(double) + 1);
+  double* Vd = (double*)malloc(kd * sizeof(double) + 1);
+  if (!Qd || !Kd || !Vd) {
+    free(Qd); free(Kd); free(Vd);
+    return -2;
+  }
+  int rc = 0;
+  for (int s = 0; s < nsel && rc == 0; ++s) {
+    const int b = sel[s] / Hq, hq = sel[s] % Hq, hkv = hq / g;
+    if (b < 0 || b >= B) { rc = -1; break; }
+    load_head(q + ((size_t)b * Hq + hq) * qd, Nq, d, Qd);
+    load_head(k + ((size_t)b * Hkv + hkv) * kd, Nk, d, Kd);
+    load_head(v + ((size_t)b * Hkv + hkv) * kd, Nk, d, Vd);
+    double* Os = O + (size_t)s * qd;
+    double* Ls = LSE + (size_t)s * Nq;
+#pragma omp parallel
+    {
+      double* p = (double*)malloc(((size_t)Nk + 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+      for (int i = 0; i < Nq; ++i) {
+        const int jend = causal ? i + off + 1 : Nk;   /* keys [0, jend) are visible */
+        const double* qrow = Qd + (size_t)i * d;
+        double m = -INFINITY;
+        for (int j = 0; j < jend; ++j) {
+          double sc = 0.0;
+          const double* krow = Kd + (size_t)j * d;
+          for (int kk = 0; kk < d; ++kk) sc += qrow[kk] * krow[kk];
+          p[j] = sc * scale;
+          if (p[j] > m) m = p[j];
+        }
+        double sum = 0.0;
+        for (int j = 0; j < jend; ++j) {
+          p[j] = exp(p[j] - m);
+          sum += p[j];
+        }
+        double* orow = Os + (size_t)i * d;
+        for (int c = 0; c < d; ++c) orow[c] = 0.0;
+        for (int j = 0; j < jend; ++j) {
+          const double w = p[j] / sum;
+          const double* vrow = Vd + (size_t)j * d;
+          for (int c = 0; c < d; ++c) orow[c] += w * vrow[c];
+        }
+        Ls[i] = m + log(sum);
+      }
+      free(p);
+    }
+  }
+  free(Qd); free(Kd); free(Vd);
+  return rc;
+}
