@@ -25,6 +25,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 _p, _i, _f, _ll, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
 _lib.attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]
 _lib.attn_fwd.restype = _i
+_lib.attn_fwd_kv.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+_lib.attn_fwd_kv.restype = _i
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
 _lib.attn_bwd.restype = _i
 _lib.attn_bwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
@@ -107,6 +109,28 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
         raise ValueError("lse: expected a contiguous fp32 tensor [B,Hq,N]")
     _check(_lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)),
                          float(scale), _stream(stream)))
+    return o, lse
+
+
+def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+    """O, LSE for Nq queries after a cache of Nk >= Nq keys.  q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d]
+    CUDA bf16; query i stands at key position i + Nk - Nq (causal: sees keys up to there)."""
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _dev_bf16("q", q, (B, Hq, Nq, d))
+    _dev_bf16("k", k, (B, Hkv, Nk, d))
+    _dev_bf16("v", v, (B, Hkv, Nk, d))
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _dev_bf16("o", o, (B, Hq, Nq, d))
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse: expected a contiguous fp32 tensor [B,Hq,Nq]")
+    _check(_lib.attn_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                            int(bool(causal)), float(scale), _stream(stream)))
     return o, lse
 
 

@@ -208,11 +208,17 @@ int attn_rescale_counter(int enable, unsigned long long* value_out) {
   return ATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
-             int d, int causal, float scale, void* stream) {
+// The forward for N queries against Nk keys (query i at key position i + Nk - N).
+static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                    int N, int Nk, int d, int causal, float scale, void* stream) {
   int rc = check_shape(B, Hq, Hkv, N, d, scale);
   if (rc != ATTN_OK) return rc;
+  if (Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "Nk=%d must be >= 0", Nk);
   if (B == 0 || N == 0) return ATTN_OK;
+  if (Nk == 0) return fail(ATTN_ERR_INVALID_ARG, "Nk=0 with N=%d queries: the softmax has no keys", N);
+  if (causal && N > Nk)
+    return fail(ATTN_ERR_INVALID_ARG, "causal needs N <= Nk (got N=%d, Nk=%d): the first queries would see no key",
+                N, Nk);
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(ATTN_ERR_MISALIGNED, "q, k, v, o and lse must be 16-byte aligned");
@@ -222,16 +228,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
   FwdMaps maps;
   if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) return rc;
-  if ((rc = make_map(&maps.k, k, d, N, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
-  if ((rc = make_map(&maps.v, v, d, N, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.k, k, d, Nk, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.v, v, d, Nk, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.o, o, d, N, (long long)B * Hq, "o")) != ATTN_OK) return rc;
 
   FwdParams p{};
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv;
+  p.Nk = Nk; p.koff = Nk - N;
   p.causal = causal ? 1 : 0;
   p.pair_heads = (p.g >= 2 && p.g % 2 == 0) ? 1 : 0;
   p.n_qblk = (N + 127) / 128;
-  p.n_kvblk = p.n_qblk;
+  p.n_kvblk = (Nk + 127) / 128;
   p.n_rowslots = p.pair_heads ? p.n_qblk : (p.n_qblk + 1) / 2;
   p.units_per_row = p.pair_heads ? B * (Hq / 2) : B * Hq;
   p.c = scale * 1.4426950408889634f;
@@ -259,6 +266,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   cudaError_t e = launch_fwd(maps, p, d, g_poly.load(), (int)grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return post_launch(s, st);
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, N, d, causal, scale, stream);
+}
+
+int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                int Nk, int d, int causal, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
 }
 
 int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* stream) {

@@ -134,7 +134,8 @@ __device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
     if (rows[t] >= p.N) {
       T.n[t] = 0;
     } else if (p.causal) {
-      const int last = min(rows[t] + 127, p.N - 1);
+      // the last key visible to the tile's last query
+      const int last = min(rows[t] + 127, p.N - 1) + p.koff;
       T.n[t] = last / 128 + 1;
     } else {
       T.n[t] = p.n_kvblk;
@@ -346,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence(u);
       float* s = reinterpret_cast<float*>(u);
       const int kb = j * 128;
-      const bool need_mask = (kb + 127 >= p.N) || (p.causal && kb + 127 > row0_t);
+      const bool need_mask = (kb + 127 >= p.Nk) || (p.causal && kb + 127 > row0_t + p.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(grow, p.N - 1) : p.N - 1) - kb;  // last visible column
+        const int lim = (p.causal ? min(grow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;  // last visible column
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;

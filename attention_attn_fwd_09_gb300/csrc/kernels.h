@@ -9,10 +9,11 @@
 namespace attn {
 
 struct FwdParams {
-  int B, Hq, Hkv, N, g;
+  int B, Hq, Hkv, N, g;      // N: query length
+  int Nk, koff;              // key length and Nk - N (query i stands at key position i + koff)
   int causal;
   int pair_heads;          // 1: a CTA's two tiles are query heads 2p, 2p+1 of one KV group
-  int n_qblk, n_kvblk;     // ceil(N / 128)
+  int n_qblk, n_kvblk;     // ceil(N / 128), ceil(Nk / 128)
   int units_per_row;       // CTAs per query-row slot (see fwd.cu unit mapping)
   int n_rowslots;          // query-row slots per head (pair) sequence
   int split_from;          // units >= split_from run as two one-tile CTAs (the last, partial wave)

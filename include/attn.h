@@ -65,6 +65,20 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int d, int causal, float scale, void* stream);
 
 /*
+ * Forward for Nq queries appended after a cache of Nk >= Nq keys (chunked prefill or
+ * decoding against a key/value cache: the reverse-engineering page, KV-cache inference).
+ * Query i stands at key position i + Nk - Nq; with causal it sees keys j <= i + Nk - Nq
+ * (the mask aligned at the bottom-right corner; Nq = Nk is attn_fwd).
+ *
+ *   q, o [B,Hq,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; lse [B,Hq,Nq] fp32; other arguments
+ *       and ownership as attn_fwd.
+ * Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG when Nk = 0 < Nq or when causal and
+ * Nq > Nk (the first queries would see no key).
+ */
+int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                int Nk, int d, int causal, float scale, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ accumulator
  * [B,Hq,ceil(N/128)*128,d] with each head's rows padded to whole 128-row tiles,
  * rowsum(dO o O) and LSE*log2(e) [B,Hq,N], ordering counters when deterministic).  0

@@ -1,0 +1,56 @@
+"""Forward parity with Nq queries after a cache of Nk >= Nq keys (attn_fwd_kv): the CUDA
+path against the fp64 oracle's bottom-right-aligned definition, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_inputs import default_scale, make_inputs
+from parity import check_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    import attention_attn_fwd_09_gb300 as A
+    A.attn_set_debug_knobs()
+    A.attn_device_status(True)
+    yield A
+
+
+SHAPES = [  # B, Hq, Hkv, Nq, Nk, d
+    (1, 2, 2, 1, 300, 128),      # one new token against a cache
+    (2, 4, 1, 16, 1000, 64),     # a few tokens, multi-query
+    (1, 8, 2, 128, 640, 128),    # one query tile, grouped heads (pairs share K/V)
+    (1, 4, 4, 200, 333, 128),    # ragged on both sides
+    (2, 2, 2, 257, 257, 64),     # the square case through the same entry point
+    (1, 2, 1, 130, 4096, 128),   # long cache
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dHq%dHkv%dNq%dNk%dd%d" % s)
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_shapes(A, shape, causal):
+    B, Hq, Hkv, Nq, Nk, d = shape
+    x = make_inputs(500 + Nq + Nk + d, B, Hq, Hkv, Nk, d)
+    q = x["q"][:, :, Nk - Nq:].contiguous()
+    scale = default_scale(d)
+    dev = torch.device("cuda")
+    o, lse = A.attn_fwd_kv(q.to(dev), x["k"].to(dev), x["v"].to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert A.attn_device_status(True) == 0
+    O, L = oracle.attn_fwd_kv(q, x["k"], x["v"], causal, scale)
+    check_fwd(o.float().cpu().numpy(), lse.cpu().numpy(), O, L, f"{shape} causal={causal}")
+
+
+def test_kv_square_equals_attn_fwd(A):
+    B, H, N, d = 1, 4, 300, 128
+    x = make_inputs(561, B, H, H, N, d)
+    dev = torch.device("cuda")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    for causal in (False, True):
+        o1, l1 = A.attn_fwd(q, k, v, causal=causal)
+        o2, l2 = A.attn_fwd_kv(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
