@@ -4,8 +4,9 @@ Argument marshalling only: every step of the computation runs in the library's C
 kernels.  PyTorch supplies device memory and the current stream.  If the compiled
 library is missing this module raises at import time; there is no fallback.
 
-Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_bwd``,
-``attn_bwd_workspace_size``, ``attn_last_error`` and the test/tuning knobs.
+Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_fwd_kv``, ``attn_bwd``,
+``attn_bwd_noalloc``, ``attn_bwd_workspace_size``, ``attn_last_error`` and the test/tuning
+knobs.
 """
 from __future__ import annotations
 
