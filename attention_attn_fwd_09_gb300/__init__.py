@@ -26,8 +26,10 @@ _lib = ctypes.CDLL(LIB_PATH)
 _p, _i, _f, _ll, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
 _lib.attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]
 _lib.attn_fwd.restype = _i
-_lib.attn_fwd_kv.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+_lib.attn_fwd_kv.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p]
 _lib.attn_fwd_kv.restype = _i
+_lib.attn_fwd_kv_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+_lib.attn_fwd_kv_workspace_size.restype = _sz
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
 _lib.attn_bwd.restype = _i
 _lib.attn_bwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
@@ -113,9 +115,19 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
     return o, lse
 
 
-def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+def attn_fwd_kv_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    n = _lib.attn_fwd_kv_workspace_size(B, Hq, Hkv, Nq, Nk, d)
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError(-1, attn_last_error())
+    return int(n)
+
+
+def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, workspace=None,
+                stream=None):
     """O, LSE for Nq queries after a cache of Nk >= Nq keys.  q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d]
-    CUDA bf16; query i stands at key position i + Nk - Nq (causal: sees keys up to there)."""
+    CUDA bf16; query i stands at key position i + Nk - Nq (causal: sees keys up to there).
+    ``workspace``: a uint8 CUDA tensor of at least attn_fwd_kv_workspace_size(...) bytes
+    (allocated here when None and needed; pass an empty tensor to use the ordinary tiling)."""
     B, Hq, Nq, d = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     _dev_bf16("q", q, (B, Hq, Nq, d))
@@ -130,8 +142,13 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None, o=Non
     _dev_bf16("o", o, (B, Hq, Nq, d))
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse: expected a contiguous fp32 tensor [B,Hq,Nq]")
+    if workspace is None:
+        n = attn_fwd_kv_workspace_size(B, Hq, Hkv, Nq, Nk, d)
+        workspace = torch.empty((n,), dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace.numel() > 0 else ctypes.c_void_p(0)
     _check(_lib.attn_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                            int(bool(causal)), float(scale), _stream(stream)))
+                            int(bool(causal)), float(scale), ws_ptr, workspace.numel() * workspace.element_size(),
+                            _stream(stream)))
     return o, lse
 
 

@@ -99,12 +99,15 @@ EncodeFn get_encode() {
 }
 
 // [BH, rows, d] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
-int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, const char* name) {
+// box_rows x box_planes: 128 x 1 for ordinary tiles; N x g to gather the g query heads of
+// a group (rows h * N + q) into one tile in grouped decode mode.
+int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, const char* name, int box_rows = 128,
+             int box_planes = 1) {
   EncodeFn enc = get_encode();
   if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(g_encode_err));
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * (cuuint64_t)d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -208,9 +211,34 @@ int attn_rescale_counter(int enable, unsigned long long* value_out) {
   return ATTN_OK;
 }
 
+// Grouped decode plan for N queries after Nk keys: used when a group's g query heads x N
+// queries fit one 128-row tile (g >= 2); the keys are split so that the grid about fills
+// the GPU once.  pack = 0 means the ordinary path.
+struct KvPlan {
+  int pack, splits, blocks_per_split;
+  size_t ws_bytes;
+};
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+static KvPlan kv_plan(int B, int Hq, int Hkv, int N, int Nk, int d, int sms) {
+  KvPlan k{0, 1, 0, 0};
+  const int g = Hq / Hkv;
+  if (B <= 0 || N <= 0 || Nk <= 0 || g < 2 || (long long)g * N > 128) return k;
+  const int nkv = (Nk + 127) / 128;
+  const long long units = (long long)B * Hkv;
+  long long sp = std::min<long long>(nkv, std::max<long long>(1, sms / units));
+  const int bps = (int)((nkv + sp - 1) / sp);
+  sp = (nkv + bps - 1) / bps;   // every split holds at least one key block
+  k.pack = 1;
+  k.splits = (int)sp;
+  k.blocks_per_split = bps;
+  k.ws_bytes = al256((size_t)sp * units * 128 * d * 4) + al256((size_t)sp * units * 128 * 4);
+  return k;
+}
+
 // The forward for N queries against Nk keys (query i at key position i + Nk - N).
 static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                    int N, int Nk, int d, int causal, float scale, void* stream) {
+                    int N, int Nk, int d, int causal, float scale, void* workspace, size_t ws_bytes,
+                    void* stream) {
   int rc = check_shape(B, Hq, Hkv, N, d, scale);
   if (rc != ATTN_OK) return rc;
   if (Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "Nk=%d must be >= 0", Nk);
@@ -225,9 +253,15 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   int dev = 0;
   const DevSyms* s = dev_syms(&dev);
   if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+  const KvPlan plan = kv_plan(B, Hq, Hkv, N, Nk, d, std::max(1, s->sms));
+  const bool pack = plan.pack && workspace != nullptr && ws_bytes >= plan.ws_bytes && aligned16(workspace);
 
   FwdMaps maps;
-  if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) return rc;
+  if (pack) {
+    if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q", N, Hq / Hkv)) != ATTN_OK) return rc;
+  } else if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) {
+    return rc;
+  }
   if ((rc = make_map(&maps.k, k, d, Nk, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.v, v, d, Nk, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.o, o, d, N, (long long)B * Hq, "o")) != ATTN_OK) return rc;
@@ -260,22 +294,44 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
     if (units >= sms && rem > 0 && 2 * rem <= sms) p.split_from = (int)(units - rem);
     else if (units < sms && 2 * units <= sms) p.split_from = 0;
   }
-  const long long grid = p.split_from + 2 * (units - p.split_from);
+  long long grid = p.split_from + 2 * (units - p.split_from);
+  p.q_tile_bytes = (unsigned)((d / 64) * 128 * 128);
+  if (pack) {
+    p.pack = 1;
+    p.kv_splits = plan.splits;
+    p.blocks_per_split = plan.blocks_per_split;
+    p.q_tile_bytes = (unsigned)((d / 64) * 128 * N * p.g);   // NCH boxes of 64 columns x N rows x g heads
+    char* w = static_cast<char*>(workspace);
+    p.part_o = reinterpret_cast<float*>(w);
+    p.part_lse = reinterpret_cast<float*>(w + al256((size_t)plan.splits * B * Hkv * 128 * d * 4));
+    grid = (long long)B * Hkv * plan.splits;
+  }
   if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_fwd(maps, p, d, g_poly.load(), (int)grid, st);
+  cudaError_t e = launch_fwd(maps, p, d, pack ? 0 : g_poly.load(), (int)grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (pack && (e = launch_fwd_merge(p, d, o, st)) != cudaSuccess) return cuda_fail(e, "forward merge launch");
   return post_launch(s, st);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
              int d, int causal, float scale, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, N, d, causal, scale, stream);
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, N, d, causal, scale, nullptr, 0, stream);
+}
+
+size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128)) {
+    set_last_error("attn_fwd_kv_workspace_size: invalid sizes");
+    return (size_t)-1;
+  }
+  const DevSyms* s = dev_syms(nullptr);
+  const int sms = s->err == cudaSuccess ? std::max(1, s->sms) : 1;
+  return kv_plan(B, Hq, Hkv, Nq, Nk, d, sms).ws_bytes;
 }
 
 int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                int Nk, int d, int causal, float scale, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, stream);
+                int Nk, int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, workspace, workspace_bytes, stream);
 }
 
 int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* stream) {

@@ -98,12 +98,29 @@ __device__ __forceinline__ constexpr bool poly_lane(int i) {
 struct Tiles {
   int n[2];       // key blocks per tile (0 = tile absent)
   int row0[2];    // first query row of each tile
-  int bh[2];      // b * Hq + hq of each tile
+  int bh[2];      // b * Hq + hq of each tile (grouped decode: the group's first head)
   int bkv;        // b * Hkv + hkv
+  int j0;         // first key block (grouped decode: the start of this CTA's key split)
 };
+
+// Grouped decode mode: CTA = (K/V head, key split); its one tile holds the group's
+// g query heads x N queries as rows h * N + q.
+__device__ __forceinline__ Tiles map_unit_grouped(const FwdParams& p, int cta) {
+  Tiles T;
+  const int unit = cta / p.kv_splits, sp = cta % p.kv_splits;
+  const int b = unit / p.Hkv, hkv = unit % p.Hkv;
+  T.bkv = unit;
+  T.bh[0] = T.bh[1] = b * p.Hq + hkv * p.g;
+  T.row0[0] = T.row0[1] = 0;
+  T.j0 = sp * p.blocks_per_split;
+  T.n[0] = min(p.n_kvblk, T.j0 + p.blocks_per_split) - T.j0;
+  T.n[1] = 0;
+  return T;
+}
 
 __device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
   Tiles T;
+  T.j0 = 0;
   int hu, rs;
   if (p.causal) {  // longest rows first
     rs = p.n_rowslots - 1 - unit / p.units_per_row;
@@ -145,7 +162,8 @@ __device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
   return T;
 }
 
-template <int D, int POLY>
+// MODE 0: the standard forward; MODE 1: grouped decode (partial results to the workspace).
+template <int D, int POLY, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -169,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTAs past split_from each take one tile of a unit (the other half of the unit goes to
   // the next CTA); the lone tile always sits in slot 0.
   Tiles T;
-  if ((int)blockIdx.x < p.split_from) {
+  if constexpr (MODE == 1) {
+    T = map_unit_grouped(p, blockIdx.x);
+  } else if ((int)blockIdx.x < p.split_from) {
     T = map_unit(p, blockIdx.x);
   } else {
     const int k = (int)blockIdx.x - p.split_from;
@@ -223,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      const uint32_t qbytes = (T.n[0] > 0 ? C::TILE : 0) + (T.n[1] > 0 ? C::TILE : 0);
+      const uint32_t qtile = MODE == 1 ? p.q_tile_bytes : C::TILE;
+      const uint32_t qbytes = (T.n[0] > 0 ? qtile : 0) + (T.n[1] > 0 ? qtile : 0);
       mbar_arrive_expect_tx(BAR(B_Q), qbytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -252,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(B_FULL + slot), C::TILE);
           const CUtensorMap* tm = which ? &tm_v : &tm_k;
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, T.bkv,
+            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, (T.j0 + j) * 128, T.bkv,
                         BAR(B_FULL + slot));
         }
       }
@@ -346,10 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(u);
       float* s = reinterpret_cast<float*>(u);
-      const int kb = j * 128;
-      const bool need_mask = (kb + 127 >= p.Nk) || (p.causal && kb + 127 > row0_t + p.koff);
+      const int kb = (T.j0 + j) * 128;
+      // Grouped decode: row = h * N + q holds query q (rows past g * N are padding).
+      const int qrow = MODE == 1 ? row % p.N : grow;
+      const bool need_mask =
+          MODE == 1 || (kb + 127 >= p.Nk) || (p.causal && kb + 127 > row0_t + p.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(grow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;  // last visible column
+        const int lim = (p.causal ? min(qrow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;  // last visible column
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -380,7 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the bf16 rounding error of each block's largest p: when a row's weight sits on one
       // key and the maximum is stale (that p is not exactly 1), the PV product uses
       // bf16(p), and dividing by the matching sum makes O exact up to the output rounding.
-      const float neg_m = -m;
+      // Grouped decode: a row may see no key of this CTA's key range yet (m = -inf); its
+      // probabilities are then 0, not 2^(-inf + inf).
+      const float neg_m = (MODE == 1 && m == -INFINITY) ? 0.f : -m;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
@@ -462,6 +488,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mrow = m_fin[t * 128 + row], lrow = l_fin[t * 128 + row];
       const float inv = 1.f / lq_fin[t * 128 + row];
       const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
+      if constexpr (MODE == 1) {
+        // This key split's partial result: O / lq (0 where the row saw no key) and LSE, fp32,
+        // for rows h * N + q of the group; rows past g * N are padding and not written.
+        const int unit = blockIdx.x / p.kv_splits, sp = blockIdx.x % p.kv_splits;
+        const size_t slot = (size_t)sp * (p.B * p.Hkv) + unit;
+        const bool real = row < p.g * p.N;
+        const float lqr = lq_fin[t * 128 + row];
+        const float invp = lqr > 0.f ? 1.f / lqr : 0.f;
+        float* dst = p.part_o + (slot * 128 + row) * D;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          tmem_ld32(tO + q * 32, r);   // warp-collective: every lane loads its row
+          tmem_wait_ld();
+          reg_fence(r);
+          if (real) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + q * 32 + i) =
+                  make_float4(__uint_as_float(r[i]) * invp, __uint_as_float(r[i + 1]) * invp,
+                              __uint_as_float(r[i + 2]) * invp, __uint_as_float(r[i + 3]) * invp);
+          }
+        }
+        if (real) p.part_lse[slot * 128 + row] = lrow > 0.f ? (mrow + __log2f(lrow)) * kLn2 : -INFINITY;
+        continue;
+      }
       uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
       uint32_t r[32];
 #pragma unroll 1
@@ -501,9 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int POLY>
+template <int D, int POLY, int MODE = 0>
 cudaError_t launch_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
-  auto kern = attn_fwd_kernel<D, POLY>;
+  auto kern = attn_fwd_kernel<D, POLY, MODE>;
   constexpr uint32_t smem = FwdCfg<D>::SMEM;
   static std::once_flag flags[64];
   int dev = 0;
@@ -523,6 +575,11 @@ cudaError_t launch_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_
 size_t fwd_smem_bytes(int D) { return D == 64 ? FwdCfg<64>::SMEM : FwdCfg<128>::SMEM; }
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly, int grid, cudaStream_t s) {
+  if (p.pack) {   // grouped decode: the MUFU exponential only
+    if (D == 64) return launch_t<64, 0, 1>(maps, p, grid, s);
+    if (D == 128) return launch_t<128, 0, 1>(maps, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
   if (D == 64) {
     if (poly == 0) return launch_t<64, 0>(maps, p, grid, s);
     if (poly == 4) return launch_t<64, 4>(maps, p, grid, s);
@@ -533,6 +590,59 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly,
     if (poly == 16) return launch_t<128, 16>(maps, p, grid, s);
   }
   return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------------------------
+// Grouped decode: merge the key splits.  One warp per (K/V head, row h * N + q); lane i
+// holds columns [D/32 i, D/32 (i + 1)).  LSE = ln sum_s e^LSE_s, O = sum_s e^(LSE_s - LSE) O_s.
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdParams p, uint16_t* __restrict__ o) {
+  constexpr int PER = D / 32;
+  const int gN = p.g * p.N, units = p.B * p.Hkv;
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= (long long)units * gN) return;
+  const int lane = threadIdx.x & 31;
+  const int unit = (int)(wid / gN), r = (int)(wid % gN);
+  float mx = -INFINITY;
+  for (int sp = 0; sp < p.kv_splits; ++sp)
+    mx = fmaxf(mx, p.part_lse[((size_t)sp * units + unit) * 128 + r]);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  for (int sp = 0; sp < p.kv_splits; ++sp) {
+    const size_t slot = (size_t)sp * units + unit;
+    const float ls = p.part_lse[slot * 128 + r];
+    if (ls == -INFINITY) continue;          // this split held no key visible to the row
+    const float w = __expf(ls - mx);
+    wsum += w;
+    const float* src = p.part_o + (slot * 128 + r) * D + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] += w * src[i];
+  }
+  const float inv = 1.f / wsum;
+  const int b = unit / p.Hkv, hkv = unit % p.Hkv;
+  const int h = hkv * p.g + r / p.N, q = r % p.N;
+  const size_t orow = ((size_t)(b * p.Hq + h)) * p.N + q;
+  uint32_t pk[PER / 2];
+#pragma unroll
+  for (int i = 0; i < PER / 2; ++i) pk[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  if constexpr (PER == 4) {
+    *reinterpret_cast<uint2*>(o + orow * D + lane * PER) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(o + orow * D + lane * PER) = pk[0];
+  }
+  if (lane == 0) p.lse[orow] = mx + __logf(wsum);
+}
+
+cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t s) {
+  const long long warps = (long long)p.B * p.Hkv * p.g * p.N;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  if (D == 64) fwd_merge_kernel<64><<<blocks, 256, 0, s>>>(p, static_cast<uint16_t*>(o));
+  else if (D == 128) fwd_merge_kernel<128><<<blocks, 256, 0, s>>>(p, static_cast<uint16_t*>(o));
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------

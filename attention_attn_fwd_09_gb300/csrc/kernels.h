@@ -17,6 +17,14 @@ struct FwdParams {
   int units_per_row;       // CTAs per query-row slot (see fwd.cu unit mapping)
   int n_rowslots;          // query-row slots per head (pair) sequence
   int split_from;          // units >= split_from run as two one-tile CTAs (the last, partial wave)
+  // Grouped decode mode (queries after a key cache, g * N <= 128): one CTA per (K/V head,
+  // key split) with one tile holding the group's g query heads x N queries; each CTA writes
+  // a normalised partial O and LSE for its key range, merged by launch_fwd_merge.
+  int pack;
+  int kv_splits, blocks_per_split;
+  unsigned q_tile_bytes;   // bytes one Q tile load delivers (a full tile, or g * N rows of it)
+  float* part_o;           // [kv_splits][B * Hkv][128][D] fp32
+  float* part_lse;         // [kv_splits][B * Hkv][128] fp32, natural log
   float c;                 // scale * log2(e)
   float tau;               // conditional-rescale threshold, log2 units
   float* lse;              // [B, Hq, N] fp32, natural log
@@ -34,6 +42,9 @@ struct FwdMaps {
 // the FMA polynomial instead of MUFU.EX2.
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly_per_16, int grid,
                        cudaStream_t stream);
+// Grouped decode mode: combine the kv_splits partial results into o [B,Hq,N,D] bf16 and
+// lse [B,Hq,N] fp32.
+cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
 
 // Software exp2 accuracy / throughput test entry: variant 0 = production polynomial,

@@ -72,11 +72,23 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *
  *   q, o [B,Hq,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; lse [B,Hq,Nq] fp32; other arguments
  *       and ownership as attn_fwd.
+ *   workspace: device memory of attn_fwd_kv_workspace_size(...) bytes, 16-byte aligned,
+ *       owned by the caller, or NULL.  When the g = Hq/Hkv query heads of a group times Nq
+ *       fit one 128-row tile (g >= 2, g * Nq <= 128) the call packs them into one tile per
+ *       K/V head and splits the keys over several CTAs, which needs the workspace for the
+ *       partial results; without it (NULL or too small) the ordinary tiling is used, with
+ *       the same results.
  * Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG when Nk = 0 < Nq or when causal and
  * Nq > Nk (the first queries would see no key).
  */
 int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                int Nk, int d, int causal, float scale, void* stream);
+                int Nk, int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace attn_fwd_kv uses for these sizes on the current device (0 when it
+ * packs nothing); (size_t)-1 for invalid sizes.
+ */
+size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /*
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ accumulator

@@ -18,7 +18,7 @@ def lib():
     p, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
     L.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, p]
     L.attn_fwd.restype = i
-    L.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, f, p]
+    L.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, f, p, sz, p]
     L.attn_fwd_kv.restype = i
     L.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p, sz, p]
     L.attn_bwd.restype = i
@@ -100,7 +100,7 @@ def test_exp2_entry_validates(lib):
 
 def test_fwd_kv_argument_errors(lib):
     # Checked before any device work.
-    args = lambda Nq, Nk, causal: (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, Nq, Nk, 64, causal, 0.1, None)
+    args = lambda Nq, Nk, causal: (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, Nq, Nk, 64, causal, 0.1, None, 0, None)
     assert lib.attn_fwd_kv(*args(4, 0, 0)) == -1          # queries but no keys
     assert b"no keys" in lib.attn_last_error()
     assert lib.attn_fwd_kv(*args(9, 8, 1)) == -1          # causal with more queries than keys

@@ -26,6 +26,13 @@ SHAPES = [  # B, Hq, Hkv, Nq, Nk, d
     (1, 4, 4, 200, 333, 128),    # ragged on both sides
     (2, 2, 2, 257, 257, 64),     # the square case through the same entry point
     (1, 2, 1, 130, 4096, 128),   # long cache
+    # grouped decode: the g query heads x Nq queries of a group packed into one tile,
+    # keys split over CTAs
+    (2, 8, 2, 1, 5000, 128),     # one token, g = 4
+    (1, 32, 8, 4, 2048, 128),    # 16 rows per tile
+    (1, 16, 1, 8, 1000, 64),     # multi-query: exactly 128 rows
+    (1, 8, 1, 15, 777, 128),     # 120 rows, ragged cache
+    (3, 6, 3, 3, 130, 128),      # g = 2, two key blocks
 ]
 
 
@@ -54,3 +61,20 @@ def test_kv_square_equals_attn_fwd(A):
         o2, l2 = A.attn_fwd_kv(q, k, v, causal=causal)
         torch.cuda.synchronize()
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_decode_matches_ordinary_tiling(A, causal):
+    # The packed, key-split path and the ordinary tiling (no workspace) agree.
+    B, Hq, Hkv, Nq, Nk, d = 2, 16, 4, 4, 3000, 128
+    x = make_inputs(570, B, Hq, Hkv, Nk, d)
+    dev = torch.device("cuda")
+    q = x["q"][:, :, Nk - Nq:].contiguous().to(dev)
+    k, v = x["k"].to(dev), x["v"].to(dev)
+    assert A.attn_fwd_kv_workspace_size(B, Hq, Hkv, Nq, Nk, d) > 0
+    o1, l1 = A.attn_fwd_kv(q, k, v, causal=causal)
+    o2, l2 = A.attn_fwd_kv(q, k, v, causal=causal, workspace=torch.empty(0, dtype=torch.uint8, device=dev))
+    torch.cuda.synchronize()
+    assert A.attn_device_status(True) == 0
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
