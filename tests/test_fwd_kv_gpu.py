@@ -33,6 +33,8 @@ SHAPES = [  # B, Hq, Hkv, Nq, Nk, d
     (1, 16, 1, 8, 1000, 64),     # multi-query: exactly 128 rows
     (1, 8, 1, 15, 777, 128),     # 120 rows, ragged cache
     (3, 6, 3, 3, 130, 128),      # g = 2, two key blocks
+    (1, 9, 3, 5, 500, 128),      # g = 3, 15 rows
+    (2, 5, 1, 7, 333, 64),       # odd g = 5, 35 rows
 ]
 
 
