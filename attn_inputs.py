@@ -75,3 +75,45 @@ def sweep_workload(N: int, d: int) -> dict:
 def long_bwd_workload(N: int) -> dict:
     """Backward at length: B=2, 16 heads, d=128."""
     return dict(seed=5, B=2, Hq=16, Hkv=16, N=N, d=128, recipe="normal")
+
+
+# ------------------------------------------------------------------ packed variable-length inputs
+def varlen_lengths(seed: int, total: int, lo: int, hi: int) -> list:
+    """Sequence lengths drawn i.i.d. uniform on the integers [lo, hi] (CPU generator seeded
+    with ``seed``) until they reach ``total`` tokens; the last length is cut so that the
+    lengths sum to exactly ``total``."""
+    g = torch.Generator().manual_seed(int(seed))
+    lens, acc = [], 0
+    while acc < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g).item())
+        n = min(n, total - acc)
+        lens.append(n)
+        acc += n
+    return lens
+
+
+def offsets(lens) -> torch.Tensor:
+    """Row offsets [0, l0, l0 + l1, ...] (int32) of sequences packed one after another."""
+    out = [0]
+    for n in lens:
+        out.append(out[-1] + int(n))
+    return torch.tensor(out, dtype=torch.int32)
+
+
+def make_varlen_inputs(seed: int, lens_q, lens_k, Hq: int, Hkv: int, d: int, *, recipe: str = "normal") -> dict:
+    """Packed sequences: ``q [Hq, sum(lens_q), d]``, ``k``/``v [Hkv, sum(lens_k), d]`` (CPU
+    bf16, drawn as ``make_inputs`` draws them, Q then K then V) and the int32 offsets
+    ``cu_q``/``cu_k`` (B + 1 entries each)."""
+    if len(lens_q) != len(lens_k):
+        raise ValueError("lens_q and lens_k need one entry per sequence")
+    tq, tk = sum(int(n) for n in lens_q), sum(int(n) for n in lens_k)
+    x = make_inputs(seed, 1, Hq, Hkv, max(tq, tk), d, recipe=recipe)
+    return {"q": x["q"][0, :, :tq].contiguous(), "k": x["k"][0, :, :tk].contiguous(),
+            "v": x["v"][0, :, :tk].contiguous(), "cu_q": offsets(lens_q), "cu_k": offsets(lens_k)}
+
+
+def varlen_workload() -> dict:
+    """Packed training batch of mixed lengths: 65536 tokens in sequences of 256..8192
+    tokens (uniform), 16 heads, d = 128."""
+    lens = varlen_lengths(7, 65536, 256, 8192)
+    return dict(seed=7, lens=lens, Hq=16, Hkv=16, d=128)

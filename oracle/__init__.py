@@ -4,7 +4,8 @@ Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 import this package.  The product path (the CUDA library and its Python binding) never
 imports it, and this package imports nothing from the product path.
 
-``attn_fwd`` / ``attn_bwd`` (and ``attn_fwd_kv``, queries after a longer key cache) wrap
+``attn_fwd`` / ``attn_bwd`` (and ``attn_fwd_kv``, queries after a longer key cache, and
+``attn_fwd_varlen``, packed sequences of different lengths, built on it) wrap
 the plain-C fp64 implementation in ``attn_oracle.c``
 (materialised S and P, chain-rule gradients); ``tiled`` holds a step-by-step fp32
 emulation of the tiled online softmax with the conditional rescale.
@@ -135,4 +136,41 @@ def attn_fwd_kv(q, k, v, causal: bool, scale: float, heads=None):
         raise ValueError(f"oracle_attn_fwd_kv failed ({rc})")
     if heads is None:
         return O.reshape(B, Hq, Nq, d), L.reshape(B, Hq, Nq)
+    return O, L
+
+
+def attn_fwd_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float):
+    """fp64 forward over packed variable-length sequences.
+
+    ``q [Hq, total_q, d]`` and ``k``/``v [Hkv, total_k, d]`` (bf16) hold the sequences one
+    after another along the row axis; sequence b owns query rows ``cu_q[b]:cu_q[b+1]`` and
+    key rows ``cu_k[b]:cu_k[b+1]``.  Each sequence is an attention problem of its own (the
+    packed-sequence scheduling of "FlashAttention-4 explained", section 06, changes only
+    the order in which the problems run), computed by ``attn_fwd_kv`` with B = 1, so causal
+    is aligned to the sequence's last key.  Returns O ``[Hq, total_q, d]`` and LSE
+    ``[Hq, total_q]``; rows of empty sequences do not exist, so nothing is left unset.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    cq = np.asarray(cu_q, dtype=np.int64).reshape(-1)
+    ck = np.asarray(cu_k, dtype=np.int64).reshape(-1)
+    Hq, Tq, d = qb.shape
+    Hkv, Tk = kb.shape[0], kb.shape[1]
+    if len(cq) != len(ck) or len(cq) < 1:
+        raise ValueError("cu_q and cu_k must both hold B + 1 offsets")
+    if cq[0] != 0 or ck[0] != 0 or cq[-1] != Tq or ck[-1] != Tk:
+        raise ValueError("offsets must start at 0 and end at the packed lengths")
+    if np.any(np.diff(cq) < 0) or np.any(np.diff(ck) < 0):
+        raise ValueError("offsets must not decrease")
+    O = np.zeros((Hq, Tq, d), dtype=np.float64)
+    L = np.zeros((Hq, Tq), dtype=np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            raise ValueError(f"sequence {b} has {q1 - q0} queries and no keys")
+        Ob, Lb = attn_fwd_kv(np.ascontiguousarray(qb[None, :, q0:q1]), np.ascontiguousarray(kb[None, :, k0:k1]),
+                             np.ascontiguousarray(vb[None, :, k0:k1]), causal, scale)
+        O[:, q0:q1] = Ob[0]
+        L[:, q0:q1] = Lb[0]
     return O, L
