@@ -4,9 +4,10 @@ Argument marshalling only: every step of the computation runs in the library's C
 kernels.  PyTorch supplies device memory and the current stream.  If the compiled
 library is missing this module raises at import time; there is no fallback.
 
-Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_fwd_kv``, ``attn_bwd``,
-``attn_bwd_noalloc``, ``attn_bwd_workspace_size``, ``attn_last_error`` and the test/tuning
-knobs.
+Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_fwd_kv``,
+``attn_fwd_varlen`` (packed sequences of different lengths), ``attn_bwd``,
+``attn_bwd_noalloc``, the ``*_workspace_size`` queries, ``attn_last_error`` and the
+test/tuning knobs.
 """
 from __future__ import annotations
 
@@ -30,6 +31,12 @@ _lib.attn_fwd_kv.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f,
 _lib.attn_fwd_kv.restype = _i
 _lib.attn_fwd_kv_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
 _lib.attn_fwd_kv_workspace_size.restype = _sz
+_lib.attn_fwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p]
+_lib.attn_fwd_varlen.restype = _i
+_lib.attn_fwd_varlen_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.attn_fwd_varlen_workspace_size.restype = _sz
+_lib.attn_set_varlen_order.argtypes = [_i]
+_lib.attn_set_varlen_order.restype = _i
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
 _lib.attn_bwd.restype = _i
 _lib.attn_bwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
@@ -150,6 +157,54 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None, o=Non
                             int(bool(causal)), float(scale), ws_ptr, workspace.numel() * workspace.element_size(),
                             _stream(stream)))
     return o, lse
+
+
+def attn_fwd_varlen_workspace_size(B: int, Hq: int, Hkv: int, total_q: int, d: int) -> int:
+    n = _lib.attn_fwd_varlen_workspace_size(B, Hq, Hkv, total_q, d)
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError(-1, attn_last_error())
+    return int(n)
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False, scale: float | None = None,
+                    o=None, lse=None, workspace=None, stream=None):
+    """O, LSE for packed sequences of different lengths.  q [Hq, total_q, d], k/v [Hkv,
+    total_k, d] CUDA bf16; ``cu_seqlens_q``/``cu_seqlens_k``: CUDA int32 offsets (B + 1
+    each) of the sequences along the row axis.  Within a sequence, query i stands at key
+    position i + nk - nq (causal: sees keys up to there).  ``workspace``: a uint8 CUDA
+    tensor of at least attn_fwd_varlen_workspace_size(...) bytes (allocated when None).
+    The offsets are checked on the device; a failed check shows in attn_device_status()."""
+    Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[0], k.shape[1]
+    _dev_bf16("q", q, (Hq, Tq, d))
+    _dev_bf16("k", k, (Hkv, Tk, d))
+    _dev_bf16("v", v, (Hkv, Tk, d))
+    for name, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if c.dtype != torch.int32 or not c.is_cuda or not c.is_contiguous() or c.dim() != 1:
+            raise ValueError(f"{name}: expected a contiguous 1-D CUDA int32 tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need B + 1 entries each")
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    _dev_bf16("o", o, (Hq, Tq, d))
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError("lse: expected a contiguous fp32 tensor [Hq, total_q]")
+    if workspace is None:
+        n = attn_fwd_varlen_workspace_size(B, Hq, Hkv, Tq, d)
+        workspace = torch.empty((max(n, 16),), dtype=torch.uint8, device=q.device)
+    _check(_lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                                _ptr(cu_seqlens_k), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), float(scale),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, lse
+
+
+def attn_set_varlen_order(longest_first: bool = True):
+    _check(_lib.attn_set_varlen_order(int(bool(longest_first))))
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, d: int, deterministic: bool = False) -> int:

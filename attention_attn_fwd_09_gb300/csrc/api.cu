@@ -45,6 +45,7 @@ std::atomic<long long> g_wait_ns{2000000000LL};
 std::atomic<int> g_sync_check{0};
 std::atomic<int> g_count_rescales{0};
 std::atomic<int> g_test_skip_kv{0};
+std::atomic<int> g_varlen_lpt{1};
 
 struct DevSyms {
   int* status = nullptr;
@@ -128,6 +129,13 @@ int check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
   return ATTN_OK;
 }
 
+// The error a non-zero device status word stands for.
+int status_fail(int v) {
+  if (v == DEV_BAD_OFFSETS)
+    return fail(ATTN_ERR_INVALID_ARG, "packed-sequence offsets failed the device check (device status %d)", v);
+  return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a bounded wait (device status %d)", v);
+}
+
 int post_launch(const DevSyms* s, cudaStream_t st) {
   if (!g_sync_check.load()) return ATTN_OK;
   cudaError_t e = cudaStreamSynchronize(st);
@@ -135,7 +143,7 @@ int post_launch(const DevSyms* s, cudaStream_t st) {
   int v = 0;
   e = cudaMemcpy(&v, s->status, sizeof v, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
-  if (v != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a bounded wait (device status %d)", v);
+  if (v != 0) return status_fail(v);
   return ATTN_OK;
 }
 
@@ -191,7 +199,7 @@ int attn_device_status(int clear) {
     e = cudaMemcpy(s->status, &z, sizeof z, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
   }
-  if (v != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a bounded wait (device status %d)", v);
+  if (v != 0) return status_fail(v);
   return ATTN_OK;
 }
 
@@ -332,6 +340,103 @@ size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d)
 int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                 int Nk, int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, workspace, workspace_bytes, stream);
+}
+
+// Packed variable-length sequences.  The unit table's size is bounded from the packed
+// length alone: sum_b ceil(nq_b / 128) <= floor(total_q / 128) + B tiles per head.
+static long long varlen_cap(int B, int Hq, int Hkv, int total_q) {
+  const int g = Hq / Hkv;
+  const bool pair = g >= 2 && g % 2 == 0;
+  const long long tiles = (long long)total_q / 128 + B;
+  return pair ? tiles * (Hq / 2) : ((tiles + B + 1) / 2) * Hq;
+}
+static constexpr size_t kVarlenHeader = 256;   // [0] records, [1] offsets invalid
+
+size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 || (d != 64 && d != 128)) {
+    set_last_error("attn_fwd_varlen_workspace_size: invalid sizes");
+    return (size_t)-1;
+  }
+  if (B == 0 || total_q == 0) return 0;
+  return kVarlenHeader + (size_t)varlen_cap(B, Hq, Hkv, total_q) * sizeof(int4);
+}
+
+int attn_set_varlen_order(int longest_first) {
+  g_varlen_lpt.store(longest_first ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int d, int causal,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_shape(B, Hq, Hkv, total_q, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (total_k < 0) return fail(ATTN_ERR_INVALID_ARG, "total_k=%d must be >= 0", total_k);
+  if (total_q > 0x7fffff00 || total_k > 0x7fffff00)
+    return fail(ATTN_ERR_INVALID_ARG, "packed lengths must stay below 2^31 - 256 rows");
+  if (Hq > 65535) return fail(ATTN_ERR_UNSUPPORTED, "Hq=%d: packed sequences support at most 65535 heads", Hq);
+  if (B == 0 || total_q == 0) return ATTN_OK;
+  if (total_k == 0) return fail(ATTN_ERR_INVALID_ARG, "total_k=0 with %d queries: the softmax has no keys", total_q);
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k)
+    return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_MISALIGNED, "q, k, v, o and lse must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u)
+    return fail(ATTN_ERR_MISALIGNED, "cu_seqlens_q and cu_seqlens_k must be 4-byte aligned");
+  const long long cap = varlen_cap(B, Hq, Hkv, total_q);
+  const size_t need = kVarlenHeader + (size_t)cap * sizeof(int4);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(ATTN_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  if (cap > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+  int dev = 0;
+  const DevSyms* s = dev_syms(&dev);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+
+  FwdMaps maps;
+  if ((rc = make_map(&maps.q, q, d, total_q, Hq, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.k, k, d, total_k, Hkv, "k")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.v, v, d, total_k, Hkv, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.o, o, d, total_q, Hq, "o")) != ATTN_OK) return rc;
+
+  char* w = static_cast<char*>(workspace);
+  FwdParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = total_q; p.g = Hq / Hkv;
+  p.Nk = total_k; p.koff = 0;
+  p.causal = causal ? 1 : 0;
+  p.pair_heads = (p.g >= 2 && p.g % 2 == 0) ? 1 : 0;
+  p.pack = 2;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.vl_count = reinterpret_cast<const int*>(w);
+  p.vl_units = reinterpret_cast<const int4*>(w + kVarlenHeader);
+  p.o_ptr = o;
+  p.q_tile_bytes = (unsigned)((d / 64) * 128 * 128);
+  p.c = scale * 1.4426950408889634f;
+  p.tau = g_tau.load();
+  p.lse = lse;
+  p.wait_ns = (unsigned long long)g_wait_ns.load();
+  p.status = s->status;
+  p.rescale_count = g_count_rescales.load() ? s->rescale : nullptr;
+  p.test_skip_first_kv = g_test_skip_kv.load();
+
+  VarlenSched sc{};
+  sc.cu_q = cu_seqlens_q;
+  sc.cu_k = cu_seqlens_k;
+  sc.B = B; sc.Hq = Hq; sc.pair_heads = p.pair_heads; sc.causal = p.causal;
+  sc.total_q = total_q; sc.total_k = total_k;
+  sc.nbins = (int)std::min<long long>(2LL * ((total_k + 127LL) / 128) + 1, 32768LL);
+  sc.cap = (int)cap;
+  sc.lpt = g_varlen_lpt.load();
+  sc.header = reinterpret_cast<int*>(w);
+  sc.units = reinterpret_cast<int4*>(w + kVarlenHeader);
+  sc.status = s->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_varlen_schedule(sc, st);
+  if (e != cudaSuccess) return cuda_fail(e, "unit table launch");
+  e = launch_fwd(maps, p, d, 0, (int)cap, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return post_launch(s, st);
 }
 
 int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* stream) {

@@ -97,10 +97,14 @@ __device__ __forceinline__ constexpr bool poly_lane(int i) {
 
 struct Tiles {
   int n[2];       // key blocks per tile (0 = tile absent)
-  int row0[2];    // first query row of each tile
+  int row0[2];    // first query row of each tile (packed sequences: row of the packed tensor)
   int bh[2];      // b * Hq + hq of each tile (grouped decode: the group's first head)
   int bkv;        // b * Hkv + hkv
   int j0;         // first key block (grouped decode: the start of this CTA's key split)
+  // The sequence the tiles belong to: its first query row (qs), one past its last (qend),
+  // its first key row (krow0), its number of keys (nk) and nk - nq (koff).  Constants of
+  // the launch except for packed sequences.
+  int qs, qend, krow0, nk, koff;
 };
 
 // Grouped decode mode: CTA = (K/V head, key split); its one tile holds the group's
@@ -115,12 +119,37 @@ __device__ __forceinline__ Tiles map_unit_grouped(const FwdParams& p, int cta) {
   T.j0 = sp * p.blocks_per_split;
   T.n[0] = min(p.n_kvblk, T.j0 + p.blocks_per_split) - T.j0;
   T.n[1] = 0;
+  T.qs = 0; T.qend = p.N; T.krow0 = 0; T.nk = p.Nk; T.koff = p.koff;
+  return T;
+}
+
+// Packed sequences: the CTA's record of the unit table (varlen.cu) names the sequence,
+// the two query heads and the two tiles' first rows within the sequence.
+__device__ __forceinline__ Tiles map_unit_varlen(const FwdParams& p, const int4 u) {
+  Tiles T;
+  const int b = u.x;
+  const int q0 = p.cu_q[b], nq = p.cu_q[b + 1] - q0;
+  const int k0 = p.cu_k[b], nk = p.cu_k[b + 1] - k0;
+  T.j0 = 0;
+  T.qs = q0; T.qend = q0 + nq; T.krow0 = k0; T.nk = nk; T.koff = nk - nq;
+  const int rows[2] = {u.z, u.w};
+  const int hqs[2] = {u.y & 0xffff, u.y >> 16};
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    T.row0[t] = q0 + max(rows[t], 0);
+    T.bh[t] = hqs[t];
+    if (rows[t] < 0) T.n[t] = 0;
+    else if (p.causal) T.n[t] = (min(rows[t] + 127, nq - 1) + T.koff) / 128 + 1;
+    else T.n[t] = (nk + 127) / 128;
+  }
+  T.bkv = hqs[0] / p.g;
   return T;
 }
 
 __device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
   Tiles T;
   T.j0 = 0;
+  T.qs = 0; T.qend = p.N; T.krow0 = 0; T.nk = p.Nk; T.koff = p.koff;
   int hu, rs;
   if (p.causal) {  // longest rows first
     rs = p.n_rowslots - 1 - unit / p.units_per_row;
@@ -162,7 +191,8 @@ __device__ __forceinline__ Tiles map_unit(const FwdParams& p, int unit) {
   return T;
 }
 
-// MODE 0: the standard forward; MODE 1: grouped decode (partial results to the workspace).
+// MODE 0: the standard forward; MODE 1: grouped decode (partial results to the workspace);
+// MODE 2: packed variable-length sequences (one unit-table record per CTA).
 template <int D, int POLY, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -187,7 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTAs past split_from each take one tile of a unit (the other half of the unit goes to
   // the next CTA); the lone tile always sits in slot 0.
   Tiles T;
-  if constexpr (MODE == 1) {
+  if constexpr (MODE == 2) {
+    // CTAs past the table's records have no work: they leave before touching barriers or
+    // tensor memory.
+    if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
+    T = map_unit_varlen(p, p.vl_units[blockIdx.x]);
+  } else if constexpr (MODE == 1) {
     T = map_unit_grouped(p, blockIdx.x);
   } else if ((int)blockIdx.x < p.split_from) {
     T = map_unit(p, blockIdx.x);
@@ -273,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(B_FULL + slot), C::TILE);
           const CUtensorMap* tm = which ? &tm_v : &tm_k;
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, (T.j0 + j) * 128, T.bkv,
-                        BAR(B_FULL + slot));
+            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64,
+                        T.krow0 + (T.j0 + j) * 128, T.bkv, BAR(B_FULL + slot));
         }
       }
       if (!ok) {
@@ -368,12 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence(u);
       float* s = reinterpret_cast<float*>(u);
       const int kb = (T.j0 + j) * 128;
-      // Grouped decode: row = h * N + q holds query q (rows past g * N are padding).
-      const int qrow = MODE == 1 ? row % p.N : grow;
+      // Grouped decode: row = h * N + q holds query q (rows past g * N are padding).  Packed
+      // sequences: rows and keys count from the sequence's start; the keys past its end
+      // (the next sequence's) are masked like those past the tensor's end.
+      const int qrow = MODE == 1 ? row % p.N : grow - T.qs;
       const bool need_mask =
-          MODE == 1 || (kb + 127 >= p.Nk) || (p.causal && kb + 127 > row0_t + p.koff);
+          MODE == 1 || (kb + 127 >= T.nk) || (p.causal && kb + 127 > row0_t - T.qs + T.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(qrow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;  // last visible column
+        const int lim = (p.causal ? min(qrow + T.koff, T.nk - 1) : T.nk - 1) - kb;  // last visible column
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -515,6 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       uint8_t* stage = smem + C::OFF_Q + t * C::TILE;
+      const int grow = T.row0[t] + row;
+      // Packed sequences: a tile that ends inside the packed tensor but past its sequence's
+      // last row is written row by row (a TMA store would overwrite the next sequence).
+      const bool direct = MODE == 2 && T.row0[t] + 128 > T.qend;
+      uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) + ((size_t)T.bh[t] * p.N + grow) * D;
       uint32_t r[32];
 #pragma unroll 1
       for (int q = 0; q < D / 32; ++q) {
@@ -525,6 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        if (direct) {
+          if (grow < T.qend) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(orow + q * 32 + u * 8) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+          continue;
+        }
         const int box = (q * 32) / 64, j0 = ((q * 32) % 64) / 8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -532,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(stage + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      const int grow = T.row0[t] + row;
-      if (grow < p.N) p.lse[(size_t)T.bh[t] * p.N + grow] = (mrow + __log2f(lrow)) * kLn2;
+      if (grow < T.qend) p.lse[(size_t)T.bh[t] * p.N + grow] = (mrow + __log2f(lrow)) * kLn2;
+      if (direct) continue;
       fence_proxy_async_smem();
       mbar_arrive(BAR(B_EPI + t));
       if (warp == 12 && lane == 0 && mbar_wait(BAR(B_EPI + t), 0, wc)) {
@@ -575,6 +626,11 @@ cudaError_t launch_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_
 size_t fwd_smem_bytes(int D) { return D == 64 ? FwdCfg<64>::SMEM : FwdCfg<128>::SMEM; }
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly, int grid, cudaStream_t s) {
+  if (p.pack == 2) {   // packed sequences: the MUFU exponential only
+    if (D == 64) return launch_t<64, 0, 2>(maps, p, grid, s);
+    if (D == 128) return launch_t<128, 0, 2>(maps, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
   if (p.pack) {   // grouped decode: the MUFU exponential only
     if (D == 64) return launch_t<64, 0, 1>(maps, p, grid, s);
     if (D == 128) return launch_t<128, 0, 1>(maps, p, grid, s);

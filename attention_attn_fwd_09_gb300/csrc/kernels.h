@@ -8,6 +8,11 @@
 
 namespace attn {
 
+// Device status word codes (see attn_device_status).  Kernels never trap: a kernel that
+// gives up on a bounded wait, or finds its device-side arguments invalid, writes one of
+// these and returns.
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_OFFSETS = 2 };
+
 struct FwdParams {
   int B, Hq, Hkv, N, g;      // N: query length
   int Nk, koff;              // key length and Nk - N (query i stands at key position i + koff)
@@ -20,11 +25,19 @@ struct FwdParams {
   // Grouped decode mode (queries after a key cache, g * N <= 128): one CTA per (K/V head,
   // key split) with one tile holding the group's g query heads x N queries; each CTA writes
   // a normalised partial O and LSE for its key range, merged by launch_fwd_merge.
-  int pack;
+  int pack;                // 0 ordinary, 1 grouped decode, 2 packed variable-length sequences
   int kv_splits, blocks_per_split;
   unsigned q_tile_bytes;   // bytes one Q tile load delivers (a full tile, or g * N rows of it)
   float* part_o;           // [kv_splits][B * Hkv][128][D] fp32
   float* part_lse;         // [kv_splits][B * Hkv][128] fp32, natural log
+  // Packed variable-length mode (pack == 2): Q/O [Hq, N, D], K/V [Hkv, Nk, D] with N and Nk
+  // the packed lengths; each CTA takes one record of the unit table written by
+  // launch_varlen_schedule (CTAs past *vl_count have no record and exit at once).
+  const int* cu_q;         // [B + 1] query row offsets (device)
+  const int* cu_k;         // [B + 1] key row offsets (device)
+  const int* vl_count;     // records in the table
+  const int4* vl_units;    // {b, hq0 | hq1 << 16, r0, r1}: rows r0, r1 of sequence b (r1 < 0: one tile)
+  void* o_ptr;             // O, for tiles that end inside their sequence (plain stores)
   float c;                 // scale * log2(e)
   float tau;               // conditional-rescale threshold, log2 units
   float* lse;              // [B, Hq, N] fp32, natural log
@@ -45,6 +58,21 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly_
 // Grouped decode mode: combine the kv_splits partial results into o [B,Hq,N,D] bf16 and
 // lse [B,Hq,N] fp32.
 cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t stream);
+
+// Packed variable-length mode: the unit table.  One CTA validates the offsets and writes
+// one record per CTA of the forward (two 128-row tiles of one sequence), longest first.
+struct VarlenSched {
+  const int* cu_q;
+  const int* cu_k;
+  int B, Hq, pair_heads, causal, total_q, total_k;
+  int nbins;               // work classes (key blocks of a record, clamped to nbins - 1)
+  int cap;                 // records the table can hold
+  int lpt;                 // 1: longest first; 0: every record in one class (arrival order)
+  int* header;             // [0] records written; [1] 0, or 1 when the offsets were invalid
+  int4* units;             // [cap] records
+  int* status;             // device status word (DEV_BAD_OFFSETS on invalid offsets)
+};
+cudaError_t launch_varlen_schedule(const VarlenSched& s, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
 
 // Software exp2 accuracy / throughput test entry: variant 0 = production polynomial,

@@ -9,14 +9,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "kernels.h"
+
 namespace attn {
 
-// ---------------------------------------------------------------------------------
-// Device status word.  A kernel that gives up on a wait writes a code here; the host
-// reads it through attn_device_status().  Kernels never trap.
-// ---------------------------------------------------------------------------------
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
-
+// Bounded waits: a wait that passes its limit writes DEV_TIMEOUT to the device status
+// word (kernels.h) and returns false.
 struct WaitCtl {
   unsigned long long limit_ns;  // give up after this long in one wait
   int* status;                  // global status word

@@ -1,0 +1,156 @@
+// The unit table for packed variable-length sequences: which two 128-row query tiles
+// each CTA of the forward takes, longest first.
+//
+// "FlashAttention-4 explained", section 06 (scheduling): sequences of different lengths
+// give CTAs of very different amounts of work, and starting the largest first keeps short
+// ones from leaving the last wave to a few long CTAs.  Here a CTA's work is the number of
+// 128-key blocks its tiles visit (the whole sequence's keys, or, causal, the keys up to
+// the tiles' last query), known only once the offsets are on the device, so one CTA
+// builds the order there: a counting sort over work classes, without a host round trip.
+//
+// Records: {b, hq0 | hq1 << 16, r0, r1}: tiles starting at rows r0 and r1 of sequence b
+// (query heads hq0 and hq1; r1 < 0 when the sequence's last tile has no partner).  The
+// pairing is the ordinary forward's: two query heads of one K/V group on the same rows
+// when the group size is even, otherwise two consecutive row tiles of one head.
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr int kSchedThreads = 1024;
+
+// Key blocks that a tile starting at query row r of a sequence of nq queries and nk keys
+// visits (0 for an absent tile).  Must agree with the forward's own count.
+__device__ __forceinline__ int tile_blocks(int r, int nq, int nk, int causal) {
+  if (r < 0 || r >= nq) return 0;
+  if (!causal) return (nk + 127) / 128;
+  return (min(r + 127, nq - 1) + (nk - nq)) / 128 + 1;
+}
+
+// One pass over every (sequence, row slot): PHASE 0 counts the records of each work class,
+// PHASE 1 reserves their places (hist then holds each class's next free index) and writes
+// them.  Warps take sequences, lanes take the row slots of a sequence.
+template <int PHASE>
+__device__ void visit_slots(const VarlenSched& s, int* hist) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = s.pair_heads ? s.Hq / 2 : s.Hq;   // records per row slot
+  for (int b = warp; b < s.B; b += kSchedThreads / 32) {
+    const int q0 = s.cu_q[b], nq = s.cu_q[b + 1] - q0;
+    const int nk = s.cu_k[b + 1] - s.cu_k[b];
+    const int tiles = (nq + 127) / 128;
+    const int slots = s.pair_heads ? tiles : (tiles + 1) / 2;
+    for (int sl = lane; sl < slots; sl += 32) {
+      const int r0 = s.pair_heads ? sl * 128 : sl * 256;
+      const int r1 = s.pair_heads ? r0 : (r0 + 128 < nq ? r0 + 128 : -1);
+      int work = tile_blocks(r0, nq, nk, s.causal) + tile_blocks(r1, nq, nk, s.causal);
+      work = s.lpt ? min(work, s.nbins - 1) : 0;
+      const int bin = s.nbins - 1 - work;          // ascending bins = descending work
+      if constexpr (PHASE == 0) {
+        atomicAdd(&hist[bin], per);
+      } else {
+        const int pos = atomicAdd(&hist[bin], per);
+        for (int u = 0; u < per; ++u) {
+          if (pos + u >= s.cap) break;
+          const int hq0 = s.pair_heads ? 2 * u : u;
+          const int hq1 = s.pair_heads ? 2 * u + 1 : u;
+          s.units[pos + u] = make_int4(b, hq0 | (hq1 << 16), r0, r1);
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSchedThreads, 1) varlen_schedule_kernel(const VarlenSched s) {
+  extern __shared__ int hist[];                 // [nbins]
+  __shared__ int bad;
+  __shared__ int warp_sum[kSchedThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bad = 0;
+  for (int i = tid; i < s.nbins; i += kSchedThreads) hist[i] = 0;
+  __syncthreads();
+
+  // Offsets: start at 0, never decrease, end at the packed lengths; a sequence with
+  // queries has keys, and a causal one at least as many keys as queries.  Together these
+  // keep every row the forward touches inside the packed tensors.
+  for (int b = tid; b < s.B; b += kSchedThreads) {
+    const int q0 = s.cu_q[b], q1 = s.cu_q[b + 1], k0 = s.cu_k[b], k1 = s.cu_k[b + 1];
+    bool ok = q1 >= q0 && k1 >= k0 && (q1 == q0 || k1 > k0) && (!s.causal || k1 - k0 >= q1 - q0);
+    if (b == 0) ok = ok && q0 == 0 && k0 == 0;
+    if (b == s.B - 1) ok = ok && q1 == s.total_q && k1 == s.total_k;
+    if (!ok) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      s.header[0] = 0;
+      s.header[1] = 1;
+      atomicExch(s.status, DEV_BAD_OFFSETS);
+    }
+    return;
+  }
+
+  visit_slots<0>(s, hist);
+  __syncthreads();
+
+  // Exclusive scan of the class counts: thread t owns bins [t*C, (t+1)*C).
+  const int C = (s.nbins + kSchedThreads - 1) / kSchedThreads;
+  const int lo = min(tid * C, s.nbins), hi = min(lo + C, s.nbins);
+  int mine = 0;
+  for (int i = lo; i < hi; ++i) mine += hist[i];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sum[lane] = w;                          // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - mine + (warp > 0 ? warp_sum[warp - 1] : 0);
+  const int total = warp_sum[kSchedThreads / 32 - 1];
+  for (int i = lo; i < hi; ++i) {
+    const int c = hist[i];
+    hist[i] = run;
+    run += c;
+  }
+  __syncthreads();
+
+  visit_slots<1>(s, hist);
+  if (tid == 0) {
+    s.header[0] = min(total, s.cap);
+    s.header[1] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_varlen_schedule(const VarlenSched& s, cudaStream_t stream) {
+  const size_t smem = (size_t)s.nbins * sizeof(int);
+  static std::once_flag flags[64];
+  static cudaError_t attr_err[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::call_once(flags[dev & 63], [&] {
+    attr_err[dev & 63] = cudaFuncSetAttribute(varlen_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              128 * 1024);
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+  if (smem > 128 * 1024) return cudaErrorInvalidValue;
+  varlen_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(s);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

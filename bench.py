@@ -232,6 +232,45 @@ def oracle_sample(seconds_fwd: float = 6.0, seconds_bwd: float = 8.0):
 
 
 # ------------------------------------------------------------------------------ our arm
+def varlen_lines(A, torch, dev, flush):
+    """Forward-only lines for the packed mixed-length batch (65536 tokens in sequences of
+    256..8192, 16 heads, d = 128): the tiles longest first (the library's default) and in
+    no particular order, causal and not.  FLOPs 4*d*Hq*sum(nq*nk), halved for causal."""
+    from attn_inputs import make_varlen_inputs, varlen_workload
+    w = varlen_workload()
+    x = make_varlen_inputs(w["seed"], w["lens"], w["lens"], w["Hq"], w["Hkv"], w["d"])
+    q, k, v, cq, ck = (x[n].to(dev) for n in ("q", "k", "v", "cu_q", "cu_k"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w["Hq"], q.shape[1]), dtype=torch.float32, device=dev)
+    ws = torch.empty((A.attn_fwd_varlen_workspace_size(len(w["lens"]), w["Hq"], w["Hkv"], q.shape[1], w["d"]),),
+                     dtype=torch.uint8, device=dev)
+    full = 4.0 * w["d"] * w["Hq"] * sum(n * n for n in w["lens"])
+    res = {"sequences": len(w["lens"]), "tokens": int(q.shape[1]), "min_len": min(w["lens"]),
+           "max_len": max(w["lens"])}
+    for causal in (False, True):
+        for order in (True, False):
+            A.attn_set_varlen_order(order)
+            call = lambda: A.attn_fwd_varlen(q, k, v, cq, ck, causal=causal, scale=w["d"] ** -0.5, o=o, lse=lse,
+                                             workspace=ws)
+            for _ in range(3):
+                call()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
+            for e in evs:
+                flush.fill_(1.0)
+                e[0].record()
+                call()
+                e[1].record()
+            torch.cuda.synchronize()
+            ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+            tf = full * (0.5 if causal else 1.0) / ms / 1e9
+            res[f"{'causal' if causal else 'noncausal'}_{'longest_first' if order else 'unordered'}"] = {
+                "ms": round(ms, 4), "tflops": round(tf, 1)}
+    A.attn_set_varlen_order(True)
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout or bad offsets in the packed-sequence lines")
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -400,6 +439,7 @@ def run_ours(args):
             del qs, ks, vs, os_, ls
         if A.attn_device_status(True) != 0:
             raise RuntimeError("a kernel reported a timeout in the sweep")
+        varlen = varlen_lines(A, torch, dev, flush)
 
     peaks, peak_src = measured_peaks()
     fwd_avg = statistics.mean(fwd_ms)
@@ -436,6 +476,8 @@ def run_ours(args):
         "clocks": clk.summary(),
         "fwd_sweep_d128_noncausal": sweep,
     }
+    if not args.no_sweep:
+        out["fwd_varlen_mixed_lengths"] = varlen
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()
         out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),

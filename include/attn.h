@@ -91,6 +91,46 @@ int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse
 size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /*
+ * Forward over B packed sequences of different lengths ("FlashAttention-4 explained"
+ * page, section 06: sequences of different lengths, the CTAs with the most work started
+ * first).  Each sequence is its own attention problem; sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1,
+ * and within it query i stands at key position i + nk - nq as in attn_fwd_kv (causal is
+ * aligned at the sequence's bottom-right corner; equal offsets give the usual causal mask).
+ *
+ *   q, o [Hq, total_q, d] bf16; k, v [Hkv, total_k, d] bf16; lse [Hq, total_q] fp32
+ *       (natural log): the sequences one after another along the row axis of each head.
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 arrays of B + 1 offsets, 4-byte aligned:
+ *       starting at 0, never decreasing, ending at total_q and total_k; a sequence with
+ *       queries must have keys, and with causal at least as many keys as queries.
+ *   workspace: device memory of attn_fwd_varlen_workspace_size(...) bytes, 16-byte
+ *       aligned, owned by the caller, contents on entry irrelevant (it receives the
+ *       order in which the tiles run, built on the device from the offsets).
+ *   other arguments and ownership as attn_fwd.
+ * Errors as attn_fwd, plus ATTN_ERR_WORKSPACE, ATTN_ERR_INVALID_ARG when total_k = 0 <
+ * total_q, and ATTN_ERR_UNSUPPORTED for Hq > 65535.  The offsets are checked on the
+ * device: if they break a rule above, nothing is written to o and lse and the device
+ * status word reads ATTN_ERR_INVALID_ARG (attn_device_status; returned at once when
+ * sync_check is set).
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int d, int causal,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace attn_fwd_varlen needs: a bound that depends on B, the heads and
+ * total_q only (0 when there is nothing to do); (size_t)-1 for invalid sizes.
+ */
+size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d);
+
+/*
+ * Order of attn_fwd_varlen's tiles: 1 (default) = the CTAs with the most key blocks
+ * first; 0 = no ordering (the order in which the scheduler meets the sequences).  The
+ * results are the same either way; the knob exists to measure what the ordering buys.
+ */
+int attn_set_varlen_order(int longest_first);
+
+/*
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ accumulator
  * [B,Hq,ceil(N/128)*128,d] with each head's rows padded to whole 128-row tiles,
  * rowsum(dO o O) and LSE*log2(e) [B,Hq,N], ordering counters when deterministic).  0
@@ -164,9 +204,10 @@ int attn_get_debug_knobs(float* tau, int* poly_per_16, long long* wait_limit_ns,
 int attn_set_test_hooks(int skip_first_kv_load);
 
 /*
- * Synchronises the current device and reads the device status word: ATTN_OK, or
- * ATTN_ERR_TIMEOUT if some kernel gave up on a wait since the last clear.  clear = 1
- * resets the word.
+ * Synchronises the current device and reads the device status word: ATTN_OK,
+ * ATTN_ERR_TIMEOUT if some kernel gave up on a wait since the last clear, or
+ * ATTN_ERR_INVALID_ARG if attn_fwd_varlen's offsets failed their device check.
+ * clear = 1 resets the word.
  */
 int attn_device_status(int clear);
 

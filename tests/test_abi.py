@@ -20,6 +20,10 @@ def lib():
     L.attn_fwd.restype = i
     L.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, f, p, sz, p]
     L.attn_fwd_kv.restype = i
+    L.attn_fwd_varlen.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, f, p, sz, p]
+    L.attn_fwd_varlen.restype = i
+    L.attn_fwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_fwd_varlen_workspace_size.restype = sz
     L.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p, sz, p]
     L.attn_bwd.restype = i
     L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -107,3 +111,24 @@ def test_fwd_kv_argument_errors(lib):
     assert b"N <= Nk" in lib.attn_last_error()
     assert lib.attn_fwd_kv(*args(4, -1, 0)) == -1
     assert lib.attn_fwd_kv(*args(0, 8, 1)) == 0           # nothing to do
+
+
+def test_fwd_varlen_argument_errors(lib):
+    # Host-side checks, before any device work (the offsets themselves are checked on the
+    # device).  The workspace bound: B=2 sequences, 4 heads (no head pairs), 300 rows:
+    # floor(300/128) + 2 = 4 tiles per head at most, ceil((4 + 2) / 2) = 3 records per head.
+    assert lib.attn_fwd_varlen_workspace_size(2, 4, 4, 300, 64) == 256 + 3 * 4 * 16
+    assert lib.attn_fwd_varlen_workspace_size(2, 4, 2, 300, 64) == 256 + 4 * 2 * 16   # head pairs
+    assert lib.attn_fwd_varlen_workspace_size(0, 4, 4, 300, 64) == 0
+    assert lib.attn_fwd_varlen_workspace_size(2, 4, 3, 300, 64) == ctypes.c_size_t(-1).value
+
+    def call(B=2, Hq=4, Hkv=4, tq=300, tk=300, d=64, causal=0, cu=FAKE, ws=FAKE, ws_bytes=1 << 20):
+        return lib.attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, cu, B, Hq, Hkv, tq, tk, d, causal, 0.1,
+                                   ws, ws_bytes, None)
+    assert call(d=96) == -2
+    assert call(tk=0) == -1 and b"no keys" in lib.attn_last_error()
+    assert call(Hq=70000, Hkv=70000) == -2
+    assert call(cu=ctypes.c_void_p(0x10002)) == -3
+    assert call(ws_bytes=100) == -4
+    assert call(ws=MIS) == -3
+    assert call(B=0) == 0 and call(tq=0) == 0
