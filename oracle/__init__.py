@@ -174,3 +174,63 @@ def attn_fwd_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float):
         O[:, q0:q1] = Ob[0]
         L[:, q0:q1] = Lb[0]
     return O, L
+
+
+def _f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _bwd_one_head(q, k, v, do, causal: bool, scale: float):
+    """The backward of one query head of one sequence, from the definition: q, do [nq,d],
+    k, v [nk,d] (fp64); query i sees keys j <= i + nk - nq when causal.
+    S = scale Q K^T, P = softmax(S) by rows, O = P V; dV = P^T dO, dP = dO V^T,
+    dS = P o (dP - rowsum(dO o O)), dQ = scale dS K, dK = scale dS^T Q."""
+    nq, nk = q.shape[0], k.shape[0]
+    s = scale * (q @ k.T)
+    if causal:
+        i = np.arange(nq)[:, None]
+        j = np.arange(nk)[None, :]
+        s = np.where(j <= i + (nk - nq), s, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    o = p @ v
+    dv = p.T @ do
+    dp = do @ v.T
+    ds = p * (dp - (do * o).sum(axis=1, keepdims=True))
+    return scale * (ds @ k), scale * (ds.T @ q), dv
+
+
+def attn_bwd_varlen(q, k, v, do, cu_q, cu_k, causal: bool, scale: float):
+    """fp64 backward over packed variable-length sequences (layouts and offsets as
+    ``attn_fwd_varlen``; ``do`` like ``q``).  Each sequence and query head is differentiated
+    on its own from the definition (``_bwd_one_head``, numpy fp64 matrix products); dK and
+    dV of a K/V head sum over the query heads of its group.  Keys of a sequence without
+    queries get zero gradients.  Returns dQ ``[Hq, total_q, d]``, dK and dV
+    ``[Hkv, total_k, d]``."""
+    qd, kd, vd, dd = (_f64(_bits(t)) for t in (q, k, v, do))
+    cq = np.asarray(cu_q, dtype=np.int64).reshape(-1)
+    ck = np.asarray(cu_k, dtype=np.int64).reshape(-1)
+    Hq, Tq, d = qd.shape
+    Hkv, Tk = kd.shape[0], kd.shape[1]
+    g = Hq // Hkv
+    if len(cq) != len(ck) or cq[0] != 0 or ck[0] != 0 or cq[-1] != Tq or ck[-1] != Tk:
+        raise ValueError("offsets must hold B + 1 entries from 0 to the packed lengths")
+    if np.any(np.diff(cq) < 0) or np.any(np.diff(ck) < 0):
+        raise ValueError("offsets must not decrease")
+    dQ = np.zeros((Hq, Tq, d))
+    dK = np.zeros((Hkv, Tk, d))
+    dV = np.zeros((Hkv, Tk, d))
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        if k1 == k0 or (causal and k1 - k0 < q1 - q0):
+            raise ValueError(f"sequence {b}: some query sees no key")
+        for h in range(Hq):
+            hk = h // g
+            gq, gk, gv = _bwd_one_head(qd[h, q0:q1], kd[hk, k0:k1], vd[hk, k0:k1], dd[h, q0:q1], causal, scale)
+            dQ[h, q0:q1] = gq
+            dK[hk, k0:k1] += gk
+            dV[hk, k0:k1] += gv
+    return dQ, dK, dV

@@ -93,3 +93,70 @@ def test_invalid_offsets_are_rejected():
         oracle.attn_fwd_varlen(q, k[:, :3], v[:, :3], [0, 3, 7], [0, 3, 3], False, 0.5)
     with pytest.raises(ValueError):   # causal with fewer keys than queries
         oracle.attn_fwd_varlen(q, k[:, :5], v[:, :5], [0, 3, 7], [0, 3, 5], True, 0.5)
+
+
+# ---------------------------------------------------------------------------- backward
+def _fd_loss_kv(q, k, v, do, causal, scale):
+    """L = sum(dO o O) for one head of one sequence, fp64, query i at key i + nk - nq."""
+    nq, nk = q.shape[0], k.shape[0]
+    s = scale * q @ k.T
+    if causal:
+        s = np.where(np.arange(nk)[None, :] <= np.arange(nq)[:, None] + nk - nq, s, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    return float((do * (p @ v)).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_finite_differences_more_keys_than_queries(causal):
+    # One sequence of 3 queries after 5 keys, one head: central differences of sum(dO o O).
+    x = make_varlen_inputs(450 + causal, [3], [5], 1, 1, 4)
+    do = make_varlen_inputs(451, [3], [5], 1, 1, 4)["q"]
+    scale = 0.4
+    dQ, dK, dV = oracle.attn_bwd_varlen(x["q"], x["k"], x["v"], do, x["cu_q"], x["cu_k"], causal, scale)
+    q, k, v, dd = (t[0].double().numpy() for t in (x["q"], x["k"], x["v"], do))
+    O, _ = oracle.attn_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal, scale)
+    assert abs(_fd_loss_kv(q, k, v, dd, causal, scale) - float((dd * O[0]).sum())) < 1e-12
+    h = 1e-6
+    for name, arr, grad in (("q", q, dQ[0]), ("k", k, dK[0]), ("v", v, dV[0])):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args = {"q": q, "k": k, "v": v}
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            args[name] = plus
+            lp = _fd_loss_kv(args["q"], args["k"], args["v"], dd, causal, scale)
+            args[name] = minus
+            lm = _fd_loss_kv(args["q"], args["k"], args["v"], dd, causal, scale)
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.abs(fd - grad).max() / max(1.0, np.abs(grad).max()) < 1e-6, name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_square_sequences_match_the_unpacked_oracle(causal):
+    # Each square sequence against the (separately pinned) C oracle's backward on it alone,
+    # with grouped heads (dK, dV summed over the group).
+    lens = [9, 1, 30]
+    x = make_varlen_inputs(460 + causal, lens, lens, 4, 2, 8)
+    do = make_varlen_inputs(461, lens, lens, 4, 2, 8)["q"]
+    dQ, dK, dV = oracle.attn_bwd_varlen(x["q"], x["k"], x["v"], do, x["cu_q"], x["cu_k"], causal, 0.3)
+    cq = x["cu_q"].tolist()
+    for b in range(len(lens)):
+        sl = slice(cq[b], cq[b + 1])
+        sq = lambda t: t[:, sl].unsqueeze(0).contiguous()
+        rq, rk, rv = oracle.attn_bwd(sq(x["q"]), sq(x["k"]), sq(x["v"]), sq(do), causal, 0.3)
+        np.testing.assert_allclose(dQ[:, sl], rq[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dK[:, sl], rk[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dV[:, sl], rv[0], rtol=0, atol=1e-12)
+
+
+def test_bwd_keys_without_queries_get_zero_gradients():
+    x = make_varlen_inputs(470, [4, 0, 3], [4, 6, 5], 2, 1, 4)
+    do = make_varlen_inputs(471, [4, 0, 3], [4, 6, 5], 2, 1, 4)["q"]
+    dQ, dK, dV = oracle.attn_bwd_varlen(x["q"], x["k"], x["v"], do, x["cu_q"], x["cu_k"], True, 0.5)
+    assert not dK[:, 4:10].any() and not dV[:, 4:10].any()
+    assert np.abs(dV[:, :4]).max() > 0 and np.abs(dV[:, 10:]).max() > 0
+    # rows of P sum to one: sum over keys of dV equals sum over queries of dO, per sequence
+    dof = do.double().numpy()
+    np.testing.assert_allclose(dV[0, 10:].sum(axis=0), dof[:, 4:].sum(axis=(0, 1)), atol=1e-12)
