@@ -5,7 +5,7 @@ kernels.  PyTorch supplies device memory and the current stream.  If the compile
 library is missing this module raises at import time; there is no fallback.
 
 Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_fwd_kv``,
-``attn_fwd_varlen`` (packed sequences of different lengths), ``attn_bwd``,
+``attn_fwd_varlen`` and ``attn_bwd_varlen`` (packed sequences of different lengths), ``attn_bwd``,
 ``attn_bwd_noalloc``, the ``*_workspace_size`` queries, ``attn_last_error`` and the
 test/tuning knobs.
 """
@@ -35,6 +35,11 @@ _lib.attn_fwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
 _lib.attn_fwd_varlen.restype = _i
 _lib.attn_fwd_varlen_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.attn_fwd_varlen_workspace_size.restype = _sz
+_lib.attn_bwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p,
+                                 _sz, _p]
+_lib.attn_bwd_varlen.restype = _i
+_lib.attn_bwd_varlen_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.attn_bwd_varlen_workspace_size.restype = _sz
 _lib.attn_set_varlen_order.argtypes = [_i]
 _lib.attn_set_varlen_order.restype = _i
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
@@ -201,6 +206,50 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False, s
                                 _ptr(cu_seqlens_k), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), float(scale),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return o, lse
+
+
+def attn_bwd_varlen_workspace_size(B: int, Hq: int, Hkv: int, total_q: int, total_k: int, d: int,
+                                   deterministic: bool = False) -> int:
+    n = _lib.attn_bwd_varlen_workspace_size(B, Hq, Hkv, total_q, total_k, d, int(bool(deterministic)))
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError(-1, attn_last_error())
+    return int(n)
+
+
+def attn_bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, causal: bool = False,
+                    scale: float | None = None, deterministic: bool = False, dq=None, dk=None, dv=None,
+                    workspace=None, stream=None):
+    """dQ, dK, dV over packed sequences (layouts and offsets as ``attn_fwd_varlen``; ``o``
+    and ``lse`` as it returned them, ``do`` like ``q``)."""
+    Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[0], k.shape[1]
+    for name, t, shp in (("q", q, (Hq, Tq, d)), ("o", o, (Hq, Tq, d)), ("do", do, (Hq, Tq, d)),
+                         ("k", k, (Hkv, Tk, d)), ("v", v, (Hkv, Tk, d))):
+        _dev_bf16(name, t, shp)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError("lse: expected a contiguous fp32 tensor [Hq, total_q]")
+    for name, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if c.dtype != torch.int32 or not c.is_cuda or not c.is_contiguous() or c.dim() != 1:
+            raise ValueError(f"{name}: expected a contiguous 1-D CUDA int32 tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need B + 1 entries each")
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _dev_bf16("dq", dq, (Hq, Tq, d))
+    _dev_bf16("dk", dk, (Hkv, Tk, d))
+    _dev_bf16("dv", dv, (Hkv, Tk, d))
+    if workspace is None:
+        n = attn_bwd_varlen_workspace_size(B, Hq, Hkv, Tq, Tk, d, deterministic)
+        workspace = torch.empty((max(n, 16),), dtype=torch.uint8, device=q.device)
+    _check(_lib.attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv, Tq, Tk, d,
+                                int(bool(causal)), float(scale), int(bool(deterministic)), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
 
 
 def attn_set_varlen_order(longest_first: bool = True):

@@ -423,7 +423,8 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   VarlenSched sc{};
   sc.cu_q = cu_seqlens_q;
   sc.cu_k = cu_seqlens_k;
-  sc.B = B; sc.Hq = Hq; sc.pair_heads = p.pair_heads; sc.causal = p.causal;
+  sc.backward = 0;
+  sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = p.pair_heads; sc.causal = p.causal;
   sc.total_q = total_q; sc.total_k = total_k;
   sc.nbins = (int)std::min<long long>(2LL * ((total_k + 127LL) / 128) + 1, 32768LL);
   sc.cap = (int)cap;
@@ -494,6 +495,105 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.status = s->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd(maps, p, st);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward not available for these arguments");
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return post_launch(s, st);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 || total_k < 0 || (d != 64 && d != 128)) {
+    set_last_error("attn_bwd_varlen_workspace_size: invalid sizes");
+    return (size_t)-1;
+  }
+  if (B == 0 || (total_q == 0 && total_k == 0)) return 0;
+  return bwd_varlen_layout(B, Hq, Hkv, total_q, total_k, d, deterministic).total;
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                    int Hkv, int total_q, int total_k, int d, int causal, float scale, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_shape(B, Hq, Hkv, total_q, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (total_k < 0) return fail(ATTN_ERR_INVALID_ARG, "total_k=%d must be >= 0", total_k);
+  if (total_q > 0x7fffff00 || total_k > 0x7fffff00)
+    return fail(ATTN_ERR_INVALID_ARG, "packed lengths must stay below 2^31 - 256 rows");
+  if (B == 0 || (total_q == 0 && total_k == 0)) return ATTN_OK;
+  if (total_k == 0) return fail(ATTN_ERR_INVALID_ARG, "total_k=0 with %d queries: the softmax has no keys", total_q);
+  const BwdVarlenLayout L = bwd_varlen_layout(B, Hq, Hkv, total_q, total_k, d, deterministic);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, L.total);
+  // With no queries at all the query-side tensors are empty and may be NULL.
+  if (total_q == 0) {
+    q = o = dout = k;
+    dq = const_cast<void*>(k);
+    lse = static_cast<const float*>(k);
+  }
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
+    return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return fail(ATTN_ERR_MISALIGNED, "every tensor and the workspace must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u)
+    return fail(ATTN_ERR_MISALIGNED, "cu_seqlens_q and cu_seqlens_k must be 4-byte aligned");
+  if (L.cap > 0x7fffffffLL || (long long)Hq * L.sem_stride > 0x7fffffffLL)
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+  int dev = 0;
+  const DevSyms* s = dev_syms(&dev);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+  // Tensor maps over the packed views (with no queries, one-row maps that are never read).
+  BwdMaps maps;
+  const int tq = std::max(total_q, 1), tk = total_k;
+  if ((rc = make_map(&maps.q, q, d, tq, Hq, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dout, dout, d, tq, Hq, "dout")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.k, k, d, tk, Hkv, "k")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.v, v, d, tk, Hkv, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dk, dk, d, tk, Hkv, "dk")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dv, dv, d, tk, Hkv, "dv")) != ATTN_OK) return rc;
+
+  char* w = static_cast<char*>(workspace);
+  BwdParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = total_q; p.g = Hq / Hkv; p.D = d;
+  p.causal = causal ? 1 : 0;
+  p.deterministic = deterministic ? 1 : 0;
+  p.scale = scale;
+  p.c = scale * 1.4426950408889634f;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  p.delta = reinterpret_cast<float*>(w + L.delta);
+  p.lse2 = reinterpret_cast<float*>(w + L.lse2);
+  p.sem = deterministic ? reinterpret_cast<int*>(w + L.sem) : nullptr;
+  p.wait_ns = (unsigned long long)g_wait_ns.load();
+  p.status = s->status;
+  p.varlen = 1;
+  p.total_k = total_k;
+  p.sem_stride = L.sem_stride;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.vl_count = reinterpret_cast<const int*>(w + L.table);
+  p.vl_units = reinterpret_cast<const int4*>(w + L.table + kVarlenHeader);
+
+  VarlenSched sc{};
+  sc.cu_q = cu_seqlens_q;
+  sc.cu_k = cu_seqlens_k;
+  sc.backward = 1;
+  sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = 0; sc.causal = p.causal;
+  sc.total_q = total_q; sc.total_k = total_k;
+  sc.nbins = (int)std::min<long long>((long long)p.g * ((long long)total_q / 128 + 1) + 1, 32768LL);
+  sc.cap = (int)L.cap;
+  sc.lpt = g_varlen_lpt.load();
+  sc.header = reinterpret_cast<int*>(w + L.table);
+  sc.units = reinterpret_cast<int4*>(w + L.table + kVarlenHeader);
+  sc.status = s->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_varlen_schedule(sc, st);
+  if (e != cudaSuccess) return cuda_fail(e, "unit table launch");
+  e = launch_bwd(maps, p, st);
   if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward not available for these arguments");
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return post_launch(s, st);

@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "kernels.h"
@@ -42,6 +43,29 @@ size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int determinist
   size_t n = align256(nq * 128 * d * 4) + 2 * align256(rows * 4);
   if (deterministic) n += align256(nq * 4);
   return n;
+}
+
+BwdVarlenLayout bwd_varlen_layout(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic) {
+  BwdVarlenLayout L{};
+  // Sequence b's accumulator rows start at cu_q[b] + 128 b: its last tile's padding fits
+  // before the next sequence.  A tile id floor((cu_q[b] + 128 b) / 128) + m is unique per
+  // (sequence, tile) and at most rows_pad / 128.
+  L.rows_pad = (long long)total_q + 128LL * B;
+  L.sem_stride = (int)(L.rows_pad / 128 + 1);
+  L.cap = (long long)Hkv * ((long long)total_k / 128 + B);   // >= Hkv * sum_b ceil(nk_b / 128)
+  size_t off = 0;
+  L.dq_acc = off;
+  off += align256((size_t)Hq * L.rows_pad * d * 4);
+  L.delta = off;
+  off += align256((size_t)Hq * total_q * 4);
+  L.lse2 = off;
+  off += align256((size_t)Hq * total_q * 4);
+  L.sem = off;
+  if (deterministic) off += align256((size_t)Hq * L.sem_stride * 4);
+  L.table = off;
+  off += 256 + (size_t)L.cap * 16;
+  L.total = off;
+  return L;
 }
 
 void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int deterministic, BwdParams* p) {
@@ -62,6 +86,18 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Packed sequences: the sequence holding packed row r (0 <= r < cu[B]): the b with
+// cu[b] <= r < cu[b + 1] (empty sequences are skipped).  Always in [0, B - 1].
+__device__ __forceinline__ int seq_of(const int* __restrict__ cu, int B, int r) {
+  int lo = 1, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) > r) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo - 1;
+}
+
 // ------------------------------------------------------------------------------------
 // Preprocess: one 16-thread group per row (d = 128: 8 bf16 per thread; d = 64: 4).
 // ------------------------------------------------------------------------------------
@@ -71,7 +107,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
                                                               const float* __restrict__ lse, float* __restrict__ delta,
                                                               float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                               int* __restrict__ sem, long long rows, int N, int npad,
-                                                              int n_sem) {
+                                                              int n_sem, const int* __restrict__ cu_q, int nseq,
+                                                              long long rows_pad) {
   constexpr int PER = D / 16;  // elements per thread
   const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
   const int sub = threadIdx.x & 15;
@@ -103,7 +140,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
   const long long bh = row / N, r = row - bh * N;
-  float4* z = reinterpret_cast<float4*>(dq_acc + (bh * npad + r) * D + sub * PER);
+  // Packed sequences (cu_q set): row r of sequence b sits at r + 128 b of its head's rows.
+  const long long zrow = cu_q ? bh * rows_pad + r + 128LL * seq_of(cu_q, nseq, (int)r) : bh * npad + r;
+  float4* z = reinterpret_cast<float4*>(dq_acc + zrow * D + sub * PER);
 #pragma unroll
   for (int i = 0; i < PER / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (sub == 0) {
@@ -117,10 +156,12 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 // ------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                           float scale, long long n8, int N, int npad) {
+                                                           float scale, long long n8, int N, int npad,
+                                                           const int* __restrict__ cu_q, int nseq, long long rows_pad) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / (D / 8), bh = row / N;
-    const long long src = ((bh * npad + (row - bh * N)) * D) / 8 + i % (D / 8);
+    const long long row = i / (D / 8), bh = row / N, rr = row - bh * N;
+    const long long arow = cu_q ? bh * rows_pad + rr + 128LL * seq_of(cu_q, nseq, (int)rr) : bh * npad + rr;
+    const long long src = (arow * D) / 8 + i % (D / 8);
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * src];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * src + 1];
     uint4 r;
@@ -232,13 +273,28 @@ struct BwdKernelArgs {
   unsigned long long wait_ns;
   int* status;
 };
+// Packed sequences (the VL kernels): N = total_q; see BwdParams.  A separate type, so that
+// the other kernels' parameters stay as they are.
+struct BwdKernelArgsVL : BwdKernelArgs {
+  int total_k, sem_stride;
+  long long rows_pad;
+  const int* cu_q;
+  const int* cu_k;
+  const int* vl_count;
+  const int4* vl_units;
+  uint16_t* dk;          // for key blocks that end past their sequence (row stores)
+  uint16_t* dv;
+};
 
-template <int D>
+// VL: packed sequences; the CTA's key block, sequence and K/V head come from its record
+// of the unit table, rows count from the sequence's start, keys past its end are masked
+// and a block that runs past the end stores dK and dV row by row.
+template <int D, bool VL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                    const BwdKernelArgs a) {
+                    const std::conditional_t<VL, BwdKernelArgsVL, BwdKernelArgs> a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,15 +308,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* vec_d = vec_lse + 128;
 
   const int warp = warp_id(), lane = lane_id();
-  // Causal: key block n has nq - n query tiles, so blocks are launched in order of n
-  // across all heads (longest first).  Otherwise the blocks of one head run together
-  // and share its Q and dO tiles in L2.
-  const int nbkv = a.B * a.Hkv;
-  const int bkv = a.causal ? blockIdx.x % nbkv : blockIdx.x / a.nkb;
-  const int n = a.causal ? blockIdx.x / nbkv : blockIdx.x % a.nkb;
-  const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
-  const int m0 = a.causal ? n : 0;
-  const int n_m = a.nq - m0;
+  // The sequence: first query row q0, nqs queries in nqt tiles, first key row k0, nks keys,
+  // koff = nks - nqs (query i stands at key i + koff).  Constants of the launch unless VL.
+  int b, hkv, n, bkv, q0 = 0, nqs = a.N, k0 = 0, nks = a.N, koff = 0, nqt = a.nq;
+  if constexpr (VL) {
+    // CTAs past the table's records have no work: they leave before touching barriers or
+    // tensor memory.
+    if ((int)blockIdx.x >= __ldg(a.vl_count)) return;
+    const int4 u = a.vl_units[blockIdx.x];
+    b = u.x;
+    hkv = u.y;
+    n = u.z;
+    q0 = a.cu_q[b];
+    nqs = a.cu_q[b + 1] - q0;
+    k0 = a.cu_k[b];
+    nks = a.cu_k[b + 1] - k0;
+    koff = nks - nqs;
+    nqt = (nqs + 127) / 128;
+    bkv = hkv;                                     // K/V plane of the packed tensor maps
+  } else {
+    // Causal: key block n has nq - n query tiles, so blocks are launched in order of n
+    // across all heads (longest first).  Otherwise the blocks of one head run together
+    // and share its Q and dO tiles in L2.
+    const int nbkv = a.B * a.Hkv;
+    bkv = a.causal ? blockIdx.x % nbkv : blockIdx.x / a.nkb;
+    n = a.causal ? blockIdx.x / nbkv : blockIdx.x % a.nkb;
+    b = bkv / a.Hkv;
+    hkv = bkv % a.Hkv;
+  }
+  // First query tile that sees the block (causal: query i sees keys <= i + koff).
+  const int m0 = a.causal ? (VL ? max(0, n * 128 - koff) / 128 : n) : 0;
+  const int n_m = nqt - m0;
   const int n_iter = a.g * n_m;
   WaitCtl wc{a.wait_ns, a.status, abort_flag};
 
@@ -295,13 +373,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   //  - otherwise: one descending tile order shared by all key blocks of a head (causal
   //    blocks end at their diagonal), tile m taking blocks 0, 1, 2, ...; block n reaches
   //    each tile in the same iteration as block n - 1 and waits for that block's adds.
+  //  Packed sequences use the shared order when deterministic; otherwise non-causal
+  //  blocks start at tile n mod nqt and causal ones at their first tile.
   const bool shared_order = a.deterministic && !a.det_rotate;
-  const int m_start = shared_order ? a.nq - 1 : n, m_step = shared_order ? -1 : 1;
+  const int m_start = shared_order ? nqt - 1 : (VL ? (a.causal ? m0 : (nqt > 0 ? n % nqt : 0)) : n);
+  const int m_step = shared_order ? -1 : 1;
   auto iter_head_row = [&](int it, int& bh, int& m) {
     const int r = it / n_m;
     m = m_start + m_step * (it - r * n_m);
-    if (m >= a.nq) m -= a.nq;                        // non-causal rotation wraps around
-    bh = b * a.Hq + hkv * a.g + r;
+    if (m >= nqt) m -= nqt;                          // non-causal rotation wraps around
+    bh = (VL ? 0 : b * a.Hq) + hkv * a.g + r;
   };
 
   // Register split (per thread): warpgroup 0 (producer, MMA) 88, the two compute
@@ -320,8 +401,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(W_KV), 2 * C::TILE);
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::CHUNK, &tm_k, c * 64, n * 128, bkv, BAR(W_KV));
-        tma_load_3d(sbase + C::OFF_V + c * C::CHUNK, &tm_v, c * 64, n * 128, bkv, BAR(W_KV));
+        tma_load_3d(sbase + C::OFF_K + c * C::CHUNK, &tm_k, c * 64, k0 + n * 128, bkv, BAR(W_KV));
+        tma_load_3d(sbase + C::OFF_V + c * C::CHUNK, &tm_v, c * 64, k0 + n * 128, bkv, BAR(W_KV));
       }
       int next = 0;
       bool ok = true;
@@ -333,8 +414,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t qs = sbase + C::OFF_STAGE + st * 2 * C::TILE;
         mbar_arrive_expect_tx(BAR(W_FULL + st), 2 * C::TILE);
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(qs + c * C::CHUNK, &tm_q, c * 64, m * 128, bh, BAR(W_FULL + st));
-          tma_load_3d(qs + C::TILE + c * C::CHUNK, &tm_do, c * 64, m * 128, bh, BAR(W_FULL + st));
+          tma_load_3d(qs + c * C::CHUNK, &tm_q, c * 64, q0 + m * 128, bh, BAR(W_FULL + st));
+          tma_load_3d(qs + C::TILE + c * C::CHUNK, &tm_do, c * 64, q0 + m * 128, bh, BAR(W_FULL + st));
         }
         next = it + 1;
       }
@@ -416,7 +497,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // -LSE2 and -D of each tile's 128 queries (lane + 32u), fetched into registers one
     // tile ahead so that their global-memory latency hides behind the current tile, and
     // written to shared memory once both compute warpgroups are done with the previous
-    // ones.  Queries past N get -inf / 0, which makes their probabilities and dS zero.
+    // ones.  Queries past the sequence's end (past N, or the next packed sequence's) get
+    // -inf / 0, which makes their probabilities and dS zero.
     float nl[4], nd[4];
     auto fetch = [&](int it) {
       int bh, m;
@@ -424,8 +506,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int qj = m * 128 + u * 32 + lane;
-        nl[u] = qj < a.N ? -a.lse2[(size_t)bh * a.N + qj] : -INFINITY;
-        nd[u] = qj < a.N ? -a.delta[(size_t)bh * a.N + qj] : 0.f;
+        nl[u] = qj < nqs ? -a.lse2[(size_t)bh * a.N + q0 + qj] : -INFINITY;
+        nd[u] = qj < nqs ? -a.delta[(size_t)bh * a.N + q0 + qj] : 0.f;
       }
     };
     if (n_iter > 0) fetch(0);
@@ -459,9 +541,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!warp_wait_b(BAR(W_VFULL), it & 1, wc)) { ok = false; break; }
       if (!warp_wait_b(BAR(W_S), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
-      // Visible queries for this key row: qj >= kr when causal, qj < N, and the key itself < N.
-      const int qmin = (a.causal ? kr - m * 128 : 0) - h * 64;   // this half's columns below qmin are masked
-      const bool key_ok = kr < a.N;
+      // Visible queries for this key row: qj + koff >= kr when causal, qj < nqs (through
+      // the vectors), and the key itself < nks.
+      const int qmin = (a.causal ? kr - koff - m * 128 : 0) - h * 64;   // this half's columns below qmin are masked
+      const bool key_ok = kr < nks;
       const bool need_mask = qmin > 0 || !key_ok;
       const float4* nl4 = reinterpret_cast<const float4*>(vec_lse + h * 64);
       const float4* nd4 = reinterpret_cast<const float4*>(vec_d + h * 64);
@@ -536,25 +619,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // Epilogue: dV and scale * dK -> bf16 -> stage 0 buffers -> TMA store, once every MMA
     // has completed (the last loads into the stage buffers have then been consumed).
+    // Packed sequences: a block that runs past its sequence's last key is written row by
+    // row from registers (a TMA store would overwrite the next sequence's first rows), and
+    // a block no query sees (a sequence with keys but no queries) writes zeros.
     if (h == 0 && ok && warp_wait_b(BAR(W_DONE), 0, wc)) {
       tc_fence_after();
       uint8_t* sv = smem + C::OFF_STAGE;
       uint8_t* sk = sv + C::TILE;
+      const bool direct = VL && n * 128 + 128 > nks;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t tsrc = (which ? tdK : tdV) + lane_off;
         const float mul = which ? a.scale : 1.f;
         uint8_t* dst = which ? sk : sv;
+        uint16_t* grow = nullptr;
+        if constexpr (VL) grow = (which ? a.dk : a.dv) + ((size_t)bkv * a.total_k + k0 + kr) * D;
 #pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
           uint32_t r[32];
-          tmem_ld32(tsrc + q * 32, r);
-          tmem_wait_ld();
-          reg_fence_b(r);
+          if (VL && n_iter == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          } else {
+            tmem_ld32(tsrc + q * 32, r);
+            tmem_wait_ld();
+            reg_fence_b(r);
+          }
           uint32_t pkk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pkk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+          if (direct) {
+            if (kr < nks) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(grow + q * 32 + u * 8) =
+                    make_uint4(pkk[4 * u], pkk[4 * u + 1], pkk[4 * u + 2], pkk[4 * u + 3]);
+            }
+            continue;
+          }
           const int box = q >> 1, j0 = (q & 1) * 4;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -563,15 +666,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(BAR(W_EPI));
-      if (warp == 4 && lane == 0 && mbar_wait(BAR(W_EPI), 0, wc)) {
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_store_3d(&tm_dv, sbase + C::OFF_STAGE + c * C::CHUNK, c * 64, n * 128, bkv);
-          tma_store_3d(&tm_dk, sbase + C::OFF_STAGE + C::TILE + c * C::CHUNK, c * 64, n * 128, bkv);
+      if (!direct) {
+        fence_proxy_async_smem();
+        mbar_arrive(BAR(W_EPI));
+        if (warp == 4 && lane == 0 && mbar_wait(BAR(W_EPI), 0, wc)) {
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_store_3d(&tm_dv, sbase + C::OFF_STAGE + c * C::CHUNK, c * 64, k0 + n * 128, bkv);
+            tma_store_3d(&tm_dk, sbase + C::OFF_STAGE + C::TILE + c * C::CHUNK, c * 64, k0 + n * 128, bkv);
+          }
+          tma_store_commit();
+          tma_store_wait_all();
         }
-        tma_store_commit();
-        tma_store_wait_all();
       }
     }
   } else {
@@ -602,7 +707,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(BAR(W_DQFREE));
-      int* sem = a.deterministic ? a.sem + (size_t)bh * a.nq + m : nullptr;
+      // Packed sequences: the counters of a sequence's tiles start at (q0 + 128 b) / 128.
+      int* sem = nullptr;
+      if (a.deterministic) {
+        if constexpr (VL) sem = a.sem + (size_t)bh * a.sem_stride + (q0 + 128 * b) / 128 + m;
+        else sem = a.sem + (size_t)bh * a.nq + m;
+      }
       if (a.deterministic) {
         // This block's turn among the tile's contributions (see the tile order above).
         const int turn = a.det_rotate ? it - (it / n_m) * n_m : n;
@@ -620,8 +730,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
       }
       if (has_col) {
-        // Rows are padded to whole tiles, so queries past N add into padding rows.
-        float* dst = a.dq_acc + ((size_t)bh * a.nq * 128 + (size_t)m * 128) * D + dcol;
+        // Rows are padded to whole tiles, so queries past N (or past the sequence) add into
+        // padding rows, which are never read.  Packed sequences: a sequence's rows start at
+        // q0 + 128 b of its head's rows.
+        size_t arow;
+        if constexpr (VL) arow = (size_t)bh * a.rows_pad + q0 + 128 * (size_t)b + (size_t)m * 128;
+        else arow = (size_t)bh * a.nq * 128 + (size_t)m * 128;
+        float* dst = a.dq_acc + arow * D + dcol;
         red_add_rows<D>(dst, v, std::make_integer_sequence<int, 8>{});
       }
       if (a.deterministic) {
@@ -645,62 +760,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 }  // namespace
 
-template <int D>
+template <int D, bool VL>
 static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) {
-  const long long rows = (long long)p.B * p.Hq * p.N;
+  // Packed sequences: N is total_q and B the number of sequences, so a head has N rows.
+  const long long rows = VL ? (long long)p.Hq * p.N : (long long)p.B * p.Hq * p.N;
   const int nq = (p.N + 127) / 128;
-  const int n_sem = p.deterministic ? p.B * p.Hq * nq : 0;
+  const int n_sem = !p.deterministic ? 0 : VL ? p.Hq * p.sem_stride : p.B * p.Hq * nq;
+  const long long rows_pad = VL ? (long long)p.N + 128LL * p.B : 0;
+  const int* cu_q = VL ? p.cu_q : nullptr;
   {
     const long long blocks = std::max((rows + 15) / 16, ((long long)n_sem + 255) / 256);
-    bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
-        static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.delta, p.lse2, p.dq_acc,
-        p.sem, rows, p.N, nq * 128, n_sem);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (blocks > 0) {
+      bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
+          static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.delta, p.lse2, p.dq_acc,
+          p.sem, rows, p.N, nq * 128, n_sem, cu_q, p.B, rows_pad);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
+  int dev = 0, sms = 152;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   {
-    auto kern = attn_bwd_kernel<D>;
+    auto kern = attn_bwd_kernel<D, VL>;
     constexpr uint32_t smem = BwdCfg<D>::SMEM;
     static std::once_flag flags[64];
     static cudaError_t attr_err[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
     std::call_once(flags[dev & 63], [&] {
       attr_err[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
-    BwdKernelArgs a{};
+    std::conditional_t<VL, BwdKernelArgsVL, BwdKernelArgs> a{};
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nq;
     a.causal = p.causal; a.deterministic = p.deterministic;
-    {
-      int sms = 0;
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      a.det_rotate = (p.deterministic && !p.causal && 2 * nq <= sms) ? 1 : 0;
-    }
+    a.det_rotate = (!VL && p.deterministic && !p.causal && 2 * nq <= sms) ? 1 : 0;
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
-    const long long grid = (long long)p.B * p.Hkv * nq;
-    kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    long long grid = (long long)p.B * p.Hkv * nq;
+    if constexpr (VL) {
+      a.total_k = p.total_k; a.sem_stride = p.sem_stride; a.rows_pad = rows_pad;
+      a.cu_q = p.cu_q; a.cu_k = p.cu_k; a.vl_count = p.vl_count; a.vl_units = p.vl_units;
+      a.dk = static_cast<uint16_t*>(p.dk);
+      a.dv = static_cast<uint16_t*>(p.dv);
+      grid = (long long)p.Hkv * ((long long)p.total_k / 128 + p.B);   // the unit table's bound
+    }
+    if (grid > 0) {
+      kern<<<(unsigned)grid, kBwdThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   {
     const long long n8 = rows * D / 8;
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long blocks = std::min<long long>((n8 + 255) / 256, (long long)sms * 8);
-    bwd_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, static_cast<uint16_t*>(p.dq), p.scale, n8, p.N,
-                                                            nq * 128);
+    if (blocks > 0) {
+      bwd_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, static_cast<uint16_t*>(p.dq), p.scale, n8,
+                                                              p.N, nq * 128, cu_q, p.B, rows_pad);
+    }
     return cudaGetLastError();
   }
 }
 
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream) {
-  if (p.D == 64) return launch_bwd_t<64>(maps, p, stream);
-  if (p.D == 128) return launch_bwd_t<128>(maps, p, stream);
+  if (p.varlen) {
+    if (p.D == 64) return launch_bwd_t<64, true>(maps, p, stream);
+    if (p.D == 128) return launch_bwd_t<128, true>(maps, p, stream);
+    return cudaErrorNotSupported;
+  }
+  if (p.D == 64) return launch_bwd_t<64, false>(maps, p, stream);
+  if (p.D == 128) return launch_bwd_t<128, false>(maps, p, stream);
   return cudaErrorNotSupported;
 }
 

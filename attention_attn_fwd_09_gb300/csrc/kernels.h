@@ -60,11 +60,13 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly_
 cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t stream);
 
 // Packed variable-length mode: the unit table.  One CTA validates the offsets and writes
-// one record per CTA of the forward (two 128-row tiles of one sequence), longest first.
+// one record per CTA, longest first: for the forward two 128-row query tiles of one
+// sequence, for the backward one 128-key block of one sequence and K/V head.
 struct VarlenSched {
   const int* cu_q;
   const int* cu_k;
-  int B, Hq, pair_heads, causal, total_q, total_k;
+  int backward;            // 0: forward records; 1: backward records {b, hkv, key block, 0}
+  int B, Hq, Hkv, pair_heads, causal, total_q, total_k;
   int nbins;               // work classes (key blocks of a record, clamped to nbins - 1)
   int cap;                 // records the table can hold
   int lpt;                 // 1: longest first; 0: every record in one class (arrival order)
@@ -93,12 +95,27 @@ struct BwdParams {
   int* sem;                  // deterministic-order counters
   unsigned long long wait_ns;
   int* status;
+  // Packed sequences (varlen = 1): N is total_q, Q/O/dO/dQ [Hq, total_q, D], K/V/dK/dV
+  // [Hkv, total_k, D]; dq_acc is [Hq, total_q + 128 B, D] with sequence b's rows starting
+  // at cu_q[b] + 128 b (room for its last tile's padding), sem [Hq][sem_stride].
+  int varlen, total_k, sem_stride;
+  const int* cu_q;
+  const int* cu_k;
+  const int* vl_count;
+  const int4* vl_units;      // {b, hkv, key block n, 0}
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dout, dk, dv;
 };
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic);
+// Packed sequences: workspace layout (dq_acc, delta, lse2, sem, then the unit table).
+struct BwdVarlenLayout {
+  size_t dq_acc, delta, lse2, sem, table, total;
+  long long rows_pad, cap;
+  int sem_stride;
+};
+BwdVarlenLayout bwd_varlen_layout(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
 // Points p->dq_acc, delta, lse2, sem into the caller's workspace.
 void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int deterministic, BwdParams* p);
 

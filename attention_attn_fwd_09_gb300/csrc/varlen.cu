@@ -1,5 +1,6 @@
 // The unit table for packed variable-length sequences: which two 128-row query tiles
-// each CTA of the forward takes, longest first.
+// each CTA of the forward takes, or which key block each CTA of the backward takes,
+// longest first.
 //
 // "FlashAttention-4 explained", section 06 (scheduling): sequences of different lengths
 // give CTAs of very different amounts of work, and starting the largest first keeps short
@@ -8,10 +9,12 @@
 // the tiles' last query), known only once the offsets are on the device, so one CTA
 // builds the order there: a counting sort over work classes, without a host round trip.
 //
-// Records: {b, hq0 | hq1 << 16, r0, r1}: tiles starting at rows r0 and r1 of sequence b
-// (query heads hq0 and hq1; r1 < 0 when the sequence's last tile has no partner).  The
-// pairing is the ordinary forward's: two query heads of one K/V group on the same rows
-// when the group size is even, otherwise two consecutive row tiles of one head.
+// Forward records: {b, hq0 | hq1 << 16, r0, r1}: tiles starting at rows r0 and r1 of
+// sequence b (query heads hq0 and hq1; r1 < 0 when the sequence's last tile has no
+// partner).  The pairing is the ordinary forward's: two query heads of one K/V group on
+// the same rows when the group size is even, otherwise two consecutive row tiles of one
+// head.  Backward records: {b, hkv, n, 0}: key block n of sequence b and K/V head hkv,
+// whose work is the query tiles of the group's heads that see it.
 #include <cstdint>
 #include <mutex>
 
@@ -30,35 +33,65 @@ __device__ __forceinline__ int tile_blocks(int r, int nq, int nk, int causal) {
   return (min(r + 127, nq - 1) + (nk - nq)) / 128 + 1;
 }
 
-// One pass over every (sequence, row slot): PHASE 0 counts the records of each work class,
+// One pass over every (sequence, slot): PHASE 0 counts the records of each work class,
 // PHASE 1 reserves their places (hist then holds each class's next free index) and writes
-// them.  Warps take sequences, lanes take the row slots of a sequence.
+// them.  Warps take sequences, lanes take a sequence's slots (forward: row slots, one
+// record per query head or head pair; backward: key blocks, one record per K/V head).
+// The lanes of a warp that share a class take consecutive places in lane order, one
+// atomic per class and round, and a warp's rounds follow one another, so within one
+// sequence and class a lower slot always comes first.  The deterministic backward relies
+// on this: its key block n waits for block n - 1's additions, and a lower block never has
+// less work, so block n - 1 is never placed after block n.
 template <int PHASE>
 __device__ void visit_slots(const VarlenSched& s, int* hist) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = s.pair_heads ? s.Hq / 2 : s.Hq;   // records per row slot
+  const int g = s.Hq / s.Hkv;
+  const int per = s.backward ? s.Hkv : (s.pair_heads ? s.Hq / 2 : s.Hq);
   for (int b = warp; b < s.B; b += kSchedThreads / 32) {
     const int q0 = s.cu_q[b], nq = s.cu_q[b + 1] - q0;
     const int nk = s.cu_k[b + 1] - s.cu_k[b];
     const int tiles = (nq + 127) / 128;
-    const int slots = s.pair_heads ? tiles : (tiles + 1) / 2;
-    for (int sl = lane; sl < slots; sl += 32) {
-      const int r0 = s.pair_heads ? sl * 128 : sl * 256;
-      const int r1 = s.pair_heads ? r0 : (r0 + 128 < nq ? r0 + 128 : -1);
-      int work = tile_blocks(r0, nq, nk, s.causal) + tile_blocks(r1, nq, nk, s.causal);
-      work = s.lpt ? min(work, s.nbins - 1) : 0;
-      const int bin = s.nbins - 1 - work;          // ascending bins = descending work
-      if constexpr (PHASE == 0) {
-        atomicAdd(&hist[bin], per);
-      } else {
-        const int pos = atomicAdd(&hist[bin], per);
-        for (int u = 0; u < per; ++u) {
-          if (pos + u >= s.cap) break;
-          const int hq0 = s.pair_heads ? 2 * u : u;
-          const int hq1 = s.pair_heads ? 2 * u + 1 : u;
-          s.units[pos + u] = make_int4(b, hq0 | (hq1 << 16), r0, r1);
+    const int slots = s.backward ? (nk + 127) / 128 : (s.pair_heads ? tiles : (tiles + 1) / 2);
+    for (int base = 0; base < slots; base += 32) {
+      const int sl = base + lane;
+      const bool act = sl < slots;
+      int r0 = 0, r1 = -1, work = 0;
+      if (act) {
+        if (s.backward) {
+          // key block sl meets the query tiles from the first one that sees it (causal)
+          const int m0 = s.causal ? max(0, sl * 128 - (nk - nq)) / 128 : 0;
+          r0 = sl;
+          work = g * (tiles - m0);
+        } else {
+          r0 = s.pair_heads ? sl * 128 : sl * 256;
+          r1 = s.pair_heads ? r0 : (r0 + 128 < nq ? r0 + 128 : -1);
+          work = tile_blocks(r0, nq, nk, s.causal) + tile_blocks(r1, nq, nk, s.causal);
+        }
+        work = s.lpt ? min(work, s.nbins - 1) : 0;
+      }
+      const int bin = act ? s.nbins - 1 - work : -1;   // ascending bins = descending work
+      const unsigned grp = __match_any_sync(0xffffffffu, bin);
+      const int leader = __ffs(grp) - 1;
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      int first = 0;
+      if (act && lane == leader) first = atomicAdd(&hist[bin], __popc(grp) * per);
+      first = __shfl_sync(0xffffffffu, first, leader);
+      if constexpr (PHASE == 1) {
+        if (act) {
+          const int pos = first + rank * per;
+          for (int u = 0; u < per; ++u) {
+            if (pos + u >= s.cap) break;
+            if (s.backward) {
+              s.units[pos + u] = make_int4(b, u, r0, 0);
+            } else {
+              const int hq0 = s.pair_heads ? 2 * u : u;
+              const int hq1 = s.pair_heads ? 2 * u + 1 : u;
+              s.units[pos + u] = make_int4(b, hq0 | (hq1 << 16), r0, r1);
+            }
+          }
         }
       }
+      __syncwarp();
     }
   }
 }

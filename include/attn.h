@@ -124,9 +124,38 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
 size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d);
 
 /*
- * Order of attn_fwd_varlen's tiles: 1 (default) = the CTAs with the most key blocks
- * first; 0 = no ordering (the order in which the scheduler meets the sequences).  The
- * results are the same either way; the knob exists to measure what the ordering buys.
+ * Backward over packed sequences: dQ, dK, dV of attn_fwd_varlen's O for the same offsets
+ * (the stages of attn_bwd, one sequence at a time; "FlashAttention-4 explained" page,
+ * section 06 for the longest-first order of the key blocks).
+ *
+ *   q, o, dout, dq [Hq, total_q, d] bf16; k, v, dk, dv [Hkv, total_k, d] bf16; lse
+ *       [Hq, total_q] fp32 as attn_fwd_varlen wrote it; dq, dk, dv out (overwritten).
+ *   cu_seqlens_q, cu_seqlens_k: as attn_fwd_varlen (DEVICE int32, B + 1 entries).  Keys of
+ *       a sequence without queries get dk = dv = 0.  With total_q = 0 the query-side
+ *       pointers may be NULL.
+ *   deterministic: 1 = dQ contributions are added in a fixed order (bit-identical runs).
+ *   workspace: device memory of attn_bwd_varlen_workspace_size(...) bytes, 16-byte
+ *       aligned, owned by the caller, contents on entry irrelevant.
+ * Errors as attn_bwd, plus the device check of the offsets (attn_fwd_varlen).
+ */
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                    int Hkv, int total_q, int total_k, int d, int causal, float scale, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace attn_bwd_varlen needs: fp32 dQ accumulator [Hq, total_q + 128 B, d]
+ * (each sequence's rows padded to whole 128-row tiles), rowsum(dO o O) and LSE*log2(e)
+ * [Hq, total_q], ordering counters when deterministic, and the table of key blocks.  A
+ * bound from the sizes alone; 0 when there is nothing to do, (size_t)-1 for invalid sizes.
+ */
+size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
+
+/*
+ * Order of attn_fwd_varlen's tiles and attn_bwd_varlen's key blocks: 1 (default) = the
+ * CTAs with the most work first; 0 = no ordering (the order in which the scheduler meets
+ * the sequences).  The results are the same either way; the knob exists to measure what
+ * the ordering buys.
  */
 int attn_set_varlen_order(int longest_first);
 

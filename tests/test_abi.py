@@ -24,6 +24,10 @@ def lib():
     L.attn_fwd_varlen.restype = i
     L.attn_fwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_fwd_varlen_workspace_size.restype = sz
+    L.attn_bwd_varlen.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, f, i, p, sz, p]
+    L.attn_bwd_varlen.restype = i
+    L.attn_bwd_varlen_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    L.attn_bwd_varlen_workspace_size.restype = sz
     L.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p, sz, p]
     L.attn_bwd.restype = i
     L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -132,3 +136,27 @@ def test_fwd_varlen_argument_errors(lib):
     assert call(ws_bytes=100) == -4
     assert call(ws=MIS) == -3
     assert call(B=0) == 0 and call(tq=0) == 0
+
+
+def test_bwd_varlen_workspace_and_errors(lib):
+    # Layout: dQ accumulator Hq x (total_q + 128 B) x d fp32, D and LSE2 Hq x total_q fp32
+    # (each rounded up to 256 bytes), counters Hq x ((total_q + 128 B) / 128 + 1) when
+    # deterministic, then a 256-byte header and Hkv x (total_k / 128 + B) 16-byte records.
+    al = lambda x: (x + 255) // 256 * 256
+    B, Hq, Hkv, tq, tk, d = 3, 4, 2, 500, 700, 64
+    rows_pad = tq + 128 * B
+    base = al(Hq * rows_pad * d * 4) + 2 * al(Hq * tq * 4) + 256 + Hkv * (tk // 128 + B) * 16
+    assert lib.attn_bwd_varlen_workspace_size(B, Hq, Hkv, tq, tk, d, 0) == base
+    assert lib.attn_bwd_varlen_workspace_size(B, Hq, Hkv, tq, tk, d, 1) == base + al(Hq * (rows_pad // 128 + 1) * 4)
+    assert lib.attn_bwd_varlen_workspace_size(0, Hq, Hkv, tq, tk, d, 0) == 0
+    assert lib.attn_bwd_varlen_workspace_size(B, Hq, 3, tq, tk, d, 0) == ctypes.c_size_t(-1).value
+
+    def call(tq=500, tk=700, d=64, ws=FAKE, ws_bytes=1 << 30, cu=FAKE):
+        return lib.attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cu, cu, 3, 4, 2, tq, tk, d,
+                                   0, 0.1, 0, ws, ws_bytes, None)
+    assert call(d=96) == -2
+    assert call(tk=0) == -1 and b"no keys" in lib.attn_last_error()
+    assert call(ws_bytes=1000) == -4
+    assert call(ws=MIS) == -3
+    assert call(cu=ctypes.c_void_p(0x10001)) == -3
+    assert call(tq=0, tk=0) == 0
