@@ -426,7 +426,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   sc.backward = 0;
   sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = p.pair_heads; sc.causal = p.causal;
   sc.total_q = total_q; sc.total_k = total_k;
-  sc.nbins = (int)std::min<long long>(2LL * ((total_k + 127LL) / 128) + 1, 32768LL);
+  sc.nbins = (int)std::min<long long>((total_k + 127LL) / 128 + 1, 32768LL);   // classes: a sequence's key blocks
   sc.cap = (int)cap;
   sc.lpt = g_varlen_lpt.load();
   sc.header = reinterpret_cast<int*>(w);
@@ -584,7 +584,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   sc.backward = 1;
   sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = 0; sc.causal = p.causal;
   sc.total_q = total_q; sc.total_k = total_k;
-  sc.nbins = (int)std::min<long long>((long long)p.g * ((long long)total_q / 128 + 1) + 1, 32768LL);
+  sc.nbins = (int)std::min<long long>((total_k + 127LL) / 128 + 1, 32768LL);   // classes: a sequence's key blocks
   sc.cap = (int)L.cap;
   sc.lpt = g_varlen_lpt.load();
   sc.header = reinterpret_cast<int*>(w + L.table);

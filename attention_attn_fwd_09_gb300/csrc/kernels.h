@@ -60,14 +60,14 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly_
 cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t stream);
 
 // Packed variable-length mode: the unit table.  One CTA validates the offsets and writes
-// one record per CTA, longest first: for the forward two 128-row query tiles of one
-// sequence, for the backward one 128-key block of one sequence and K/V head.
+// one record per CTA, longest sequence first: for the forward two 128-row query tiles of
+// one sequence, for the backward one 128-key block of one sequence and K/V head.
 struct VarlenSched {
   const int* cu_q;
   const int* cu_k;
   int backward;            // 0: forward records; 1: backward records {b, hkv, key block, 0}
   int B, Hq, Hkv, pair_heads, causal, total_q, total_k;
-  int nbins;               // work classes (key blocks of a record, clamped to nbins - 1)
+  int nbins;               // work classes (a sequence's key blocks, clamped to nbins - 1)
   int cap;                 // records the table can hold
   int lpt;                 // 1: longest first; 0: every record in one class (arrival order)
   int* header;             // [0] records written; [1] 0, or 1 when the offsets were invalid

@@ -233,13 +233,18 @@ def oracle_sample(seconds_fwd: float = 6.0, seconds_bwd: float = 8.0):
 
 # ------------------------------------------------------------------------------ our arm
 def varlen_lines(A, torch, dev, flush):
-    """Forward-only lines for the packed mixed-length batch (65536 tokens in sequences of
-    256..8192, 16 heads, d = 128): the tiles longest first (the library's default) and in
-    no particular order, causal and not.  FLOPs 4*d*Hq*sum(nq*nk), halved for causal."""
+    """Lines for the packed mixed-length batch (65536 tokens in sequences of 256..8192, 16
+    heads, d = 128): forward and backward, with the work longest first (the library's
+    default) and in no particular order, causal and not.  Forward FLOPs 4*d*Hq*sum(nq*nk),
+    halved for causal; backward 2.5 times that."""
     from attn_inputs import make_varlen_inputs, varlen_workload
     w = varlen_workload()
     x = make_varlen_inputs(w["seed"], w["lens"], w["lens"], w["Hq"], w["Hkv"], w["d"])
     q, k, v, cq, ck = (x[n].to(dev) for n in ("q", "k", "v", "cu_q", "cu_k"))
+    do = torch.randn(q.shape, generator=torch.Generator(device=dev).manual_seed(8), device=dev).to(torch.bfloat16)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty((A.attn_bwd_varlen_workspace_size(len(w["lens"]), w["Hq"], w["Hkv"], q.shape[1], k.shape[1],
+                                                         w["d"], False),), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((w["Hq"], q.shape[1]), dtype=torch.float32, device=dev)
     ws = torch.empty((A.attn_fwd_varlen_workspace_size(len(w["lens"]), w["Hq"], w["Hkv"], q.shape[1], w["d"]),),
@@ -247,24 +252,31 @@ def varlen_lines(A, torch, dev, flush):
     full = 4.0 * w["d"] * w["Hq"] * sum(n * n for n in w["lens"])
     res = {"sequences": len(w["lens"]), "tokens": int(q.shape[1]), "min_len": min(w["lens"]),
            "max_len": max(w["lens"])}
+    def timed(call):
+        for _ in range(3):
+            call()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
+        for e in evs:
+            flush.fill_(1.0)
+            e[0].record()
+            call()
+            e[1].record()
+        torch.cuda.synchronize()
+        return statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+
+    scale = w["d"] ** -0.5
     for causal in (False, True):
         for order in (True, False):
             A.attn_set_varlen_order(order)
-            call = lambda: A.attn_fwd_varlen(q, k, v, cq, ck, causal=causal, scale=w["d"] ** -0.5, o=o, lse=lse,
-                                             workspace=ws)
-            for _ in range(3):
-                call()
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
-            for e in evs:
-                flush.fill_(1.0)
-                e[0].record()
-                call()
-                e[1].record()
-            torch.cuda.synchronize()
-            ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
-            tf = full * (0.5 if causal else 1.0) / ms / 1e9
+            fwd = lambda: A.attn_fwd_varlen(q, k, v, cq, ck, causal=causal, scale=scale, o=o, lse=lse, workspace=ws)
+            bwd = lambda: A.attn_bwd_varlen(q, k, v, o, lse, do, cq, ck, causal=causal, scale=scale, dq=dq, dk=dk,
+                                            dv=dv, workspace=bws)
+            ms_f = timed(fwd)
+            ms_b = timed(bwd)
+            ff = full * (0.5 if causal else 1.0)
             res[f"{'causal' if causal else 'noncausal'}_{'longest_first' if order else 'unordered'}"] = {
-                "ms": round(ms, 4), "tflops": round(tf, 1)}
+                "fwd_ms": round(ms_f, 4), "fwd_tflops": round(ff / ms_f / 1e9, 1),
+                "bwd_ms": round(ms_b, 4), "bwd_tflops": round(2.5 * ff / ms_b / 1e9, 1)}
     A.attn_set_varlen_order(True)
     if A.attn_device_status(True) != 0:
         raise RuntimeError("a kernel reported a timeout or bad offsets in the packed-sequence lines")
@@ -477,7 +489,7 @@ def run_ours(args):
         "fwd_sweep_d128_noncausal": sweep,
     }
     if not args.no_sweep:
-        out["fwd_varlen_mixed_lengths"] = varlen
+        out["varlen_mixed_lengths"] = varlen
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()
         out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),
