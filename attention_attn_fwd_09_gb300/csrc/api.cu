@@ -119,11 +119,16 @@ int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, co
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
+// wide: the forward also takes d = 192 and 256 (one-tile kernel, fwd_wide.cu).
+int check_shape(int B, int Hq, int Hkv, int N, int d, float scale, bool wide = false) {
   if (B < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "B=%d and N=%d must be >= 0", B, N);
   if (Hq <= 0 || Hkv <= 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d and Hkv=%d must be >= 1", Hq, Hkv);
   if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  if (wide && (d == 192 || d == 256)) {
+  } else if (d != 64 && d != 128) {
+    return fail(ATTN_ERR_UNSUPPORTED, wide ? "head dim d=%d (supported: 64, 128, 192, 256)"
+                                           : "head dim d=%d (supported here: 64, 128)", d);
+  }
   if (!(scale > 0.0f) || !std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
   if ((long long)B * Hq > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "B*Hq too large");
   return ATTN_OK;
@@ -230,7 +235,7 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 static KvPlan kv_plan(int B, int Hq, int Hkv, int N, int Nk, int d, int sms) {
   KvPlan k{0, 1, 0, 0};
   const int g = Hq / Hkv;
-  if (B <= 0 || N <= 0 || Nk <= 0 || g < 2 || (long long)g * N > 128) return k;
+  if (B <= 0 || N <= 0 || Nk <= 0 || g < 2 || (long long)g * N > 128 || d > 128) return k;
   const int nkv = (Nk + 127) / 128;
   const long long units = (long long)B * Hkv;
   long long sp = std::min<long long>(nkv, std::max<long long>(1, sms / units));
@@ -247,7 +252,7 @@ static KvPlan kv_plan(int B, int Hq, int Hkv, int N, int Nk, int d, int sms) {
 static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                     int N, int Nk, int d, int causal, float scale, void* workspace, size_t ws_bytes,
                     void* stream) {
-  int rc = check_shape(B, Hq, Hkv, N, d, scale);
+  int rc = check_shape(B, Hq, Hkv, N, d, scale, true);
   if (rc != ATTN_OK) return rc;
   if (Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "Nk=%d must be >= 0", Nk);
   if (B == 0 || N == 0) return ATTN_OK;
@@ -304,6 +309,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   }
   long long grid = p.split_from + 2 * (units - p.split_from);
   p.q_tile_bytes = (unsigned)((d / 64) * 128 * 128);
+  const bool wide = d > 128;
+  if (wide) grid = (long long)B * Hq * p.n_qblk;   // one query tile per CTA
   if (pack) {
     p.pack = 1;
     p.kv_splits = plan.splits;
@@ -316,7 +323,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   }
   if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_fwd(maps, p, d, pack ? 0 : g_poly.load(), (int)grid, st);
+  cudaError_t e = wide ? launch_fwd_wide(maps, p, d, (int)grid, st)
+                        : launch_fwd(maps, p, d, pack ? 0 : g_poly.load(), (int)grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   if (pack && (e = launch_fwd_merge(p, d, o, st)) != cudaSuccess) return cuda_fail(e, "forward merge launch");
   return post_launch(s, st);
@@ -328,7 +336,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128)) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 ||
+      (d != 64 && d != 128 && d != 192 && d != 256)) {
     set_last_error("attn_fwd_kv_workspace_size: invalid sizes");
     return (size_t)-1;
   }

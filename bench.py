@@ -283,6 +283,37 @@ def varlen_lines(A, torch, dev, flush):
     return res
 
 
+def wide_lines(A, torch, dev, flush):
+    """Forward-only lines for wide heads (the one-tile kernel): B=2, H=16, N=8192, d = 192
+    and 256, non-causal and causal.  FLOPs 4*B*H*N^2*d, halved for causal."""
+    res = {}
+    B, H, N = 2, 16, 8192
+    for d in (192, 256):
+        g = torch.Generator(device=dev).manual_seed(9)
+        q, k, v = (torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        for causal in (False, True):
+            call = lambda: A.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, o=o, lse=lse)
+            for _ in range(3):
+                call()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
+            for e in evs:
+                flush.fill_(1.0)
+                e[0].record()
+                call()
+                e[1].record()
+            torch.cuda.synchronize()
+            ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+            tf = fwd_flops(B, H, N, d, causal) / ms / 1e9
+            res[f"d{d}_{'causal' if causal else 'noncausal'}"] = {
+                "ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_2250": round(tf / NOMINAL_PEAK_TFLOPS, 4)}
+        del q, k, v, o, lse
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout in the wide-head lines")
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -452,6 +483,7 @@ def run_ours(args):
         if A.attn_device_status(True) != 0:
             raise RuntimeError("a kernel reported a timeout in the sweep")
         varlen = varlen_lines(A, torch, dev, flush)
+        wide = wide_lines(A, torch, dev, flush)
 
     peaks, peak_src = measured_peaks()
     fwd_avg = statistics.mean(fwd_ms)
@@ -490,6 +522,7 @@ def run_ours(args):
     }
     if not args.no_sweep:
         out["varlen_mixed_lengths"] = varlen
+        out["fwd_wide_heads"] = wide
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()
         out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),

@@ -91,6 +91,12 @@ def test_bwd_workspace_and_errors(lib):
     rc = lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 128, 64, 0, 0.1, 0,
                       FAKE, 16, None)
     assert rc == -4                          # workspace too small
+    # wide heads (192, 256) have a forward only
+    for d in (192, 256):
+        rc = lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 128, d, 0, 0.1, 0,
+                          FAKE, 1 << 30, None)
+        assert rc == -2 and b"64, 128" in lib.attn_last_error()
+        assert lib.attn_bwd_workspace_size(1, 2, 2, 128, d, 0) == ctypes.c_size_t(-1).value
 
 
 def test_knobs_validate(lib):
@@ -129,7 +135,7 @@ def test_fwd_varlen_argument_errors(lib):
     def call(B=2, Hq=4, Hkv=4, tq=300, tk=300, d=64, causal=0, cu=FAKE, ws=FAKE, ws_bytes=1 << 20):
         return lib.attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, cu, B, Hq, Hkv, tq, tk, d, causal, 0.1,
                                    ws, ws_bytes, None)
-    assert call(d=96) == -2
+    assert call(d=96) == -2 and call(d=256) == -2
     assert call(tk=0) == -1 and b"no keys" in lib.attn_last_error()
     assert call(Hq=70000, Hkv=70000) == -2
     assert call(cu=ctypes.c_void_p(0x10002)) == -3
