@@ -2,7 +2,8 @@
 //
 // Same result as the forward in fwd.cu: O = softmax(scale * Q K^T [causal]) V and LSE,
 // with the scores never leaving the SM.  The pages recommend head dimensions 128 and 256
-// ("Hotelren FA4 summary", section 5; the reverse-engineering page supports up to 256).
+// ("Hotelren FA4 summary", section 6.2, item 1; the reverse-engineering page's kernel
+// launch parameters name 256 as the largest).
 //
 // Why a kernel of its own: the two-tile ping-pong of fwd.cu needs two S buffers and two O
 // accumulators in tensor memory, 2 * 128 + 2 * d columns, which is more than the 512

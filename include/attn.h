@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = -1, /* bad shape, null pointer, bad scale */
-  ATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. d not in {64,128}) */
+  ATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. a head dim the call lacks) */
   ATTN_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = -4,   /* backward workspace missing or too small */
   ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed (message has the name) */
@@ -58,6 +58,10 @@ typedef enum {
  *
  *   q   [B,Hq,N,d] bf16, in      k, v [B,Hkv,N,d] bf16, in
  *   o   [B,Hq,N,d] bf16, out     lse  [B,Hq,N] fp32, out: ln sum_j exp(S_ij)
+ *   d:      64, 128, 192 or 256.  For 192 and 256 (up to the 256 of "Hotelren FA4
+ *           summary" section 6.2, item 1) the two tiles' accumulators do not fit tensor
+ *           memory, so a CTA takes one query tile and overlaps the softmax of one key
+ *           block with the products of the next.  Backward and packed sequences: 64, 128.
  *   causal: 0 or 1 (key j visible to query i only if j <= i)
  *   scale:  softmax scale applied to Q K^T
  */
