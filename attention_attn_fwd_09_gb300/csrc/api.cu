@@ -46,6 +46,7 @@ std::atomic<int> g_sync_check{0};
 std::atomic<int> g_count_rescales{0};
 std::atomic<int> g_test_skip_kv{0};
 std::atomic<int> g_varlen_lpt{1};
+std::atomic<int> g_one_tile_d128{0};
 
 struct DevSyms {
   int* status = nullptr;
@@ -309,8 +310,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   }
   long long grid = p.split_from + 2 * (units - p.split_from);
   p.q_tile_bytes = (unsigned)((d / 64) * 128 * 128);
-  const bool wide = d > 128;
-  if (wide) grid = (long long)B * Hq * p.n_qblk;   // one query tile per CTA
+  // One query tile per CTA (fwd_wide.cu): always for d > 128, and for d = 128 when chosen.
+  const bool wide = d > 128 || (d == 128 && !pack && g_one_tile_d128.load());
+  if (wide) grid = (long long)B * Hq * p.n_qblk;
   if (pack) {
     p.pack = 1;
     p.kv_splits = plan.splits;
@@ -368,6 +370,11 @@ size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d
   }
   if (B == 0 || total_q == 0) return 0;
   return kVarlenHeader + (size_t)varlen_cap(B, Hq, Hkv, total_q) * sizeof(int4);
+}
+
+int attn_set_fwd_one_tile(int enable) {
+  g_one_tile_d128.store(enable ? 1 : 0);
+  return ATTN_OK;
 }
 
 int attn_set_varlen_order(int longest_first) {

@@ -32,37 +32,47 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct WideCfg {
+  // d = 128 (SPLIT): a key block's S product takes only 1024 tensor-core cycles, less than
+  // one warpgroup's softmax of it, so two softmax warpgroups split each block by columns
+  // (64 keys each, exchanging their row maxima) and one warpgroup does the correction.
+  // d = 192, 256: one softmax warpgroup, two correction warpgroups (half of O each).
+  static constexpr bool SPLIT = D == 128;
   static constexpr int NCH = D / 64;                    // 64-column (128-byte) chunks
   static constexpr uint32_t CHUNK = 128 * 128;          // one 128 x 64 bf16 box
   static constexpr uint32_t TILE = CHUNK * NCH;         // one 128 x D bf16 tile
-  static constexpr int NS = D == 256 ? 2 : 3;           // K/V ring slots (one tile each)
+  static constexpr int NS = D == 256 ? 2 : D == 192 ? 3 : 5;   // K/V ring slots (one tile each)
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_RING = TILE;
   static constexpr uint32_t OFF_CTRL = OFF_RING + NS * TILE;
-  static constexpr uint32_t CTRL_BYTES = 256 + (2 * 128 + 3 * 128) * 4 + 64;
+  // control block: barriers, alpha[2][128], half maxima [2][2][128], m[128], l[2][128],
+  // lq[2][128], TMEM address, abort flag
+  static constexpr uint32_t CTRL_BYTES = 256 + (256 + 512 + 128 + 256 + 256) * 4 + 64;
   static constexpr uint32_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
-  static constexpr int HALF = D / 2;                    // O columns per correction warpgroup
+  static constexpr int OCOLS = SPLIT ? D : D / 2;       // O columns per correction warpgroup
+  static constexpr int FIRST_CORR_WG = SPLIT ? 3 : 2;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
-  static_assert(D == 192 || D == 256, "wide forward: d = 192 or 256");
+  static_assert(D == 128 || D == 192 || D == 256, "one-tile forward: d = 128, 192 or 256");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(HALF % 32 == 0, "correction columns in 32-column loads");
+  static_assert(OCOLS % 32 == 0, "correction columns in 32-column loads");
 };
 
 // Barriers (8 bytes each).  Per-block barriers come in pairs indexed by the block's parity,
 // so that a waiter can never see two phases of one barrier complete at once.
 enum {
   V_Q = 0,
-  V_FULL = 1,    // +slot: a K or V tile landed (up to 3 slots)
-  V_SFULL = 4,   // +parity: S of the block complete (also frees the block's K slot)
-  V_STATS = 6,   // +parity: the block's rescale factors are in shared memory (128)
-  V_PFULL = 8,   // +parity: P written (128) and O rescaled (256)
-  V_PVD = 10,    // +parity: the block's PV product complete (also frees its V slot)
-  V_FIN = 12,    // final row statistics written (128)
-  V_EPI = 13,    // O staged in shared memory (256)
-  V_DONE = 14,
-  V_COUNT = 15
+  V_FULL = 1,    // +slot: a K or V tile landed (up to 5 slots)
+  V_SFULL = 6,   // +parity: S of the block complete (also frees the block's K slot)
+  V_STATS = 8,   // +parity: the block's rescale factors are in shared memory (128)
+  V_PFULL = 10,  // +parity: P written and O rescaled (384)
+  V_PVD = 12,    // +parity: the block's PV product complete (also frees its V slot)
+  V_FIN = 14,    // final row statistics written (by every softmax thread)
+  V_EPI = 15,    // O staged in shared memory (by every correction thread)
+  V_DONE = 16,
+  V_XCH = 17,    // +2 quarter + parity (SPLIT): both halves' row maxima of a 32-row quarter (64)
+  V_COUNT = 25
 };
+static_assert(V_COUNT * 8 <= 256, "barriers fit the control block's first 256 bytes");
 
 __device__ __forceinline__ bool warp_wait_w(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   const bool ok = mbar_wait(bar, parity, w);
@@ -118,6 +128,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                          const FwdParams p) {
   using C = WideCfg<D>;
+  static_assert(V_FULL + C::NS <= V_SFULL, "every ring slot needs its own barrier below the next group");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -125,10 +136,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t bar0 = smem_u32(ctrl);
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   float* alpha_buf = reinterpret_cast<float*>(ctrl + 256);   // [2][128]
-  float* m_fin = alpha_buf + 256;                            // [128]
-  float* l_fin = m_fin + 128;                                // [128]
-  float* lq_fin = l_fin + 128;                               // [128]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lq_fin + 128);
+  float* pm_buf = alpha_buf + 256;                           // [2][2][128] (SPLIT)
+  float* m_fin = pm_buf + 512;                               // [128]
+  float* l_fin = m_fin + 128;                                // [2][128]
+  float* lq_fin = l_fin + 256;                               // [2][128]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lq_fin + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -146,9 +158,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       mbar_init(BAR(V_PFULL + b), 384);
       mbar_init(BAR(V_PVD + b), 1);
     }
-    mbar_init(BAR(V_FIN), 128);
-    mbar_init(BAR(V_EPI), 256);
+    mbar_init(BAR(V_FIN), C::SPLIT ? 256 : 128);
+    mbar_init(BAR(V_EPI), C::SPLIT ? 128 : 256);
     mbar_init(BAR(V_DONE), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(BAR(V_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -161,9 +174,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Register split (per thread): warpgroup 0 (producer, MMA) 64, softmax 224, the two
-  // correction warpgroups 112 each: 64 + 224 + 2 x 112 = 512 = 4 x 128, the launch's
-  // 128 x 512 threads.
+  // Register split (per thread), against the launch's 128 x 512 threads:
+  //   d = 192, 256: warpgroup 0 (producer, MMA) 64, softmax 224, two correction
+  //                 warpgroups 112 each: 64 + 224 + 2 x 112 = 512 = 4 x 128;
+  //   d = 128:      warpgroup 0 64, two softmax halves 152 each, correction 144:
+  //                 64 + 2 x 152 + 144 = 512.
+  const bool softmax_wg = C::SPLIT ? (wg == 1 || wg == 2) : (wg == 1);
   if (wg == 0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
     if (warp == 0 && lane == 0) {
@@ -248,10 +264,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tc_fence_after();
         const uint32_t vbase = sbase + C::OFF_RING + vslot * C::TILE;
         const uint32_t tS = tmem + uint32_t((j & 1) * 128), tO = tmem + 256u;
+        // P of keys 16kk .. 16kk + 15: columns 8kk .. of the buffer; with SPLIT the second
+        // half's keys sit at columns 64 .. 95 (each half writes inside its own scores).
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tO, tS + (C::SPLIT && kk >= 4 ? 32 : 0) + kk * 8, sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024),
+                 C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(BAR(V_PVD + (j & 1)));
       }
       // Drain: every MMA issued above completes before TMEM is released.
@@ -260,7 +278,97 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       while (!mbar_try_wait(BAR(V_DONE), 0) && globaltimer_ns() - t0 < p.wait_ns) {
       }
     }
-  } else if (wg == 1) {
+  } else if (softmax_wg && C::SPLIT) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
+    // ------------------------------------------------------------------ softmax, one half
+    // Half h owns keys [64h, 64h + 64) of every block.  The two halves of a row exchange
+    // their maxima, so both keep the same running maximum and rescale factor; each keeps
+    // its own sums, added in the epilogue.
+    const int h = wg - 1, q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const int grow = T.row0 + row;
+    const float c = p.c;
+    float m = -INFINITY, l = 0.f, lq = 0.f;
+    for (int j = 0; j < n; ++j) {
+      if (!warp_wait_w(BAR(V_SFULL + (j & 1)), (j >> 1) & 1, wc)) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + uint32_t((j & 1) * 128 + h * 64);
+      uint32_t u[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+      tmem_wait_ld();
+      reg_fence_w(u);
+      float* s = reinterpret_cast<float*>(u);
+      const int kb = j * 128 + h * 64;
+      const bool need_mask = (kb + 63 >= p.Nk) || (p.causal && kb + 63 > T.row0 + p.koff);
+      if (need_mask) {
+        const int lim = (p.causal ? min(grow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;   // last visible column
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int i = 4; i < 60; i += 8) {
+        mx[0] = fmax3(mx[0], s[i], s[i + 1]);
+        mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+        mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+        mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+      }
+      mx[0] = fmax3(mx[0], s[60], s[61]);
+      mx[1] = fmax3(mx[1], s[62], s[63]);
+      const float own = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      float* pm = pm_buf + (j & 1) * 256;
+      pm[h * 128 + row] = own;
+      mbar_arrive(BAR(V_XCH + q4 * 2 + (j & 1)));
+      if (!warp_wait_w(BAR(V_XCH + q4 * 2 + (j & 1)), (j >> 1) & 1, wc)) break;
+      const float other = pm[(1 - h) * 128 + row];
+      const float rmax = fmaxf(own, other);
+      const float m_cand = fmaxf(m, rmax * c);
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_cand;
+      } else if (m_cand - m > p.tau) {
+        alpha = ex2_mufu(m - m_cand);
+        m = m_cand;
+      }
+      if (h == 0) {
+        alpha_buf[(j & 1) * 128 + row] = alpha;
+        mbar_arrive(BAR(V_STATS + (j & 1)));
+      }
+      const float neg_m = -m;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        float x0, x1;
+        ffma2_bc(x0, x1, s[i], s[i + 1], c, neg_m);
+        const float e0 = ex2_mufu(x0), e1 = ex2_mufu(x1);
+        pk[i >> 1] = pack_bf16x2(e0, e1);
+        const int a2 = ((i >> 1) & 1) * 2;
+        fadd2(acc[a2], acc[a2 + 1], acc[a2], acc[a2 + 1], e0, e1);
+      }
+      {
+        // The bf16 rounding of the block's largest p is taken off lq once per row, by
+        // the half that holds that maximum (the first one on a tie).
+        const bool holds_max = own == rmax && (h == 0 || other != rmax);
+        const float pmax = ex2_mufu(fmaf(rmax, c, neg_m));
+        const float pmax_q = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+        const float blk = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        l = l * alpha + blk;
+        lq = lq * alpha + (holds_max ? blk - (pmax - pmax_q) : blk);
+      }
+      tmem_st32(tS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(V_PFULL + (j & 1)));
+    }
+    if (h == 0) m_fin[row] = m;
+    l_fin[h * 128 + row] = l;
+    lq_fin[h * 128 + row] = lq;
+    mbar_arrive(BAR(V_FIN));
+  } else if (softmax_wg) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
     // ------------------------------------------------------------------ softmax
     const int row = (warp & 3) * 32 + lane;
@@ -339,12 +447,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     lq_fin[row] = lq;
     mbar_arrive(BAR(V_FIN));
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;");
+    if constexpr (C::SPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;");
+    else asm volatile("setmaxnreg.dec.sync.aligned.u32 112;");
     // ------------------------------------------------------------------ correction + epilogue
-    const int half = wg - 2;                              // O columns [half * HALF, +HALF)
+    const int half = wg - C::FIRST_CORR_WG;              // O columns [half * OCOLS, +OCOLS)
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 256u + uint32_t(half * C::HALF);
+    const uint32_t tO = tmem + lane_off + 256u + uint32_t(half * C::OCOLS);
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
       if (!warp_wait_w(BAR(V_STATS + (j & 1)), (j >> 1) & 1, wc)) {
@@ -366,7 +475,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tc_fence_after();
         uint32_t r[32];
 #pragma unroll 1
-        for (int q = 0; q < C::HALF / 32; ++q) {
+        for (int q = 0; q < C::OCOLS / 32; ++q) {
           tmem_ld32(tO + q * 32, r);
           tmem_wait_ld();
           reg_fence_w(r);
@@ -384,11 +493,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (ok && n > 0 && warp_wait_w(BAR(V_FIN), 0, wc) &&
         warp_wait_w(BAR(V_PVD + ((n - 1) & 1)), ((n - 1) >> 1) & 1, wc)) {
       tc_fence_after();
-      const float inv = 1.f / lq_fin[row];
+      const float lrow = C::SPLIT ? l_fin[row] + l_fin[128 + row] : l_fin[row];
+      const float inv = 1.f / (C::SPLIT ? lq_fin[row] + lq_fin[128 + row] : lq_fin[row]);
       uint8_t* stage = smem + C::OFF_Q;
       uint32_t r[32];
 #pragma unroll 1
-      for (int q = 0; q < C::HALF / 32; ++q) {
+      for (int q = 0; q < C::OCOLS / 32; ++q) {
         tmem_ld32(tO + q * 32, r);
         tmem_wait_ld();
         reg_fence_w(r);
@@ -396,7 +506,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        const int col = half * C::HALF + q * 32;
+        const int col = half * C::OCOLS + q * 32;
         const int box = col / 64, j0 = (col % 64) / 8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -406,10 +516,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
       const int grow = T.row0 + row;
       if (half == 0 && grow < p.N)
-        p.lse[(size_t)T.bh * p.N + grow] = (m_fin[row] + __log2f(l_fin[row])) * kLn2;
+        p.lse[(size_t)T.bh * p.N + grow] = (m_fin[row] + __log2f(lrow)) * kLn2;
       fence_proxy_async_smem();
       mbar_arrive(BAR(V_EPI));
-      if (warp == 8 && lane == 0 && mbar_wait(BAR(V_EPI), 0, wc)) {
+      if (warp == 4 * C::FIRST_CORR_WG && lane == 0 && mbar_wait(BAR(V_EPI), 0, wc)) {
         for (int c = 0; c < C::NCH; ++c)
           tma_store_3d(&tm_o, sbase + C::OFF_Q + c * C::CHUNK, c * 64, T.row0, T.bh);
         tma_store_commit();
@@ -446,6 +556,7 @@ cudaError_t launch_wide_t(const FwdMaps& m, const FwdParams& p, int grid, cudaSt
 }  // namespace
 
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t s) {
+  if (D == 128) return launch_wide_t<128>(maps, p, grid, s);
   if (D == 192) return launch_wide_t<192>(maps, p, grid, s);
   if (D == 256) return launch_wide_t<256>(maps, p, grid, s);
   return cudaErrorInvalidValue;

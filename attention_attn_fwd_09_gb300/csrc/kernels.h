@@ -76,8 +76,8 @@ struct VarlenSched {
 };
 cudaError_t launch_varlen_schedule(const VarlenSched& s, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
-// Forward for d = 192 or 256 (fwd_wide.cu): one 128-row query tile per CTA, grid = B * Hq *
-// ceil(N / 128); same parameters as launch_fwd (ordinary mode only).
+// One-tile forward (fwd_wide.cu) for d = 128, 192 or 256: one 128-row query tile per CTA,
+// grid = B * Hq * ceil(N / 128); same parameters as launch_fwd (ordinary mode only).
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t stream);
 
 // Software exp2 accuracy / throughput test entry: variant 0 = production polynomial,

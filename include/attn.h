@@ -156,6 +156,15 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
 size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
 
 /*
+ * Which forward kernel serves d = 128: 0 = two query tiles per CTA (fwd.cu), 1 = one
+ * query tile per CTA with the softmax of each key block split over two warpgroups
+ * (fwd_wide.cu, the kernel that always serves d = 192 and 256).  Same results up to the
+ * rounding of the row sums; attn_fwd_kv's grouped decode and attn_fwd_varlen keep the
+ * two-tile kernel.  A tuning knob, process-wide.
+ */
+int attn_set_fwd_one_tile(int enable);
+
+/*
  * Order of attn_fwd_varlen's tiles and attn_bwd_varlen's key blocks: 1 (default) = the
  * CTAs with the most work first; 0 = no ordering (the order in which the scheduler meets
  * the sequences).  The results are the same either way; the knob exists to measure what
