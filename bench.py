@@ -314,6 +314,74 @@ def wide_lines(A, torch, dev, flush):
     return res
 
 
+def _median_ms(torch, flush, call, reps=8, warm=3):
+    for _ in range(warm):
+        call()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for e in evs:
+        flush.fill_(1.0)
+        e[0].record()
+        call()
+        e[1].record()
+    torch.cuda.synchronize()
+    return statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+
+
+def suite_lines(A, torch, dev, flush):
+    """The measurement suite's other configurations (forward sweep over N = 512 .. 16384,
+    d = 64 and 128, causal and not; grouped / multi-query heads at N = 8192 with outlier
+    inputs; the backward at N = 8192 and 16384, atomic and deterministic).  Each line:
+    median ms over 8 calls (L2 flushed before each), TFLOP/s, and the roofline ceiling
+    min(tensor peak, arithmetic intensity x HBM bandwidth) from MEASURED_PEAKS.json."""
+    from attn_inputs import make_inputs
+    peaks, _ = measured_peaks()
+    tpeak, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+
+    def fwd_bytes(B, Hq, Hkv, N, d):
+        return 2.0 * (2 * B * Hq * N * d + 2 * B * Hkv * N * d) + 4.0 * B * Hq * N
+
+    res = {"sweep": {}, "gqa_outliers": {}, "bwd_long": {}}
+    for d in (64, 128):
+        for n in (512, 1024, 2048, 4096, 8192, 16384):
+            b = 16384 // n
+            g = torch.Generator(device=dev).manual_seed(3)
+            q, k, v = (torch.randn((b, 16, n, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+            o, lse = torch.empty_like(q), torch.empty((b, 16, n), dtype=torch.float32, device=dev)
+            for causal in (False, True):
+                ms = _median_ms(torch, flush, lambda: A.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, o=o, lse=lse))
+                fl = fwd_flops(b, 16, n, d, causal)
+                ceil = min(tpeak, fl / fwd_bytes(b, 16, 16, n, d) * hbm / 1e3)
+                res["sweep"][f"d{d}_N{n}_{'causal' if causal else 'noncausal'}"] = {
+                    "B": b, "ms": round(ms, 4), "tflops": round(fl / ms / 1e9, 1), "ceiling_tflops": round(ceil, 1)}
+            del q, k, v, o, lse
+    for hkv in (8, 1):
+        x = make_inputs(4, 2, 32, hkv, 8192, 128, recipe="outliers")
+        q, k, v = (x[nm].to(dev) for nm in ("q", "k", "v"))
+        o, lse = torch.empty_like(q), torch.empty((2, 32, 8192), dtype=torch.float32, device=dev)
+        ms = _median_ms(torch, flush, lambda: A.attn_fwd(q, k, v, causal=True, scale=128 ** -0.5, o=o, lse=lse))
+        fl = fwd_flops(2, 32, 8192, 128, True)
+        res["gqa_outliers"][f"Hq32_Hkv{hkv}_N8192_causal"] = {"ms": round(ms, 4), "tflops": round(fl / ms / 1e9, 1)}
+        del x, q, k, v, o, lse
+    for n in (8192, 16384):
+        g = torch.Generator(device=dev).manual_seed(5)
+        q, k, v, do = (torch.randn((2, 16, n, 128), generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for causal in (False, True):
+            o, lse = A.attn_fwd(q, k, v, causal=causal)
+            for det in (False, True):
+                ws = torch.empty((A.attn_bwd_workspace_size(2, 16, 16, n, 128, det),), dtype=torch.uint8, device=dev)
+                ms = _median_ms(torch, flush, lambda: A.attn_bwd(q, k, v, o, lse, do, causal=causal, deterministic=det,
+                                                                 dq=dq, dk=dk, dv=dv, workspace=ws))
+                fl = 2.5 * fwd_flops(2, 16, n, 128, causal)
+                res["bwd_long"][f"N{n}_{'causal' if causal else 'noncausal'}_{'det' if det else 'atomic'}"] = {
+                    "ms": round(ms, 4), "tflops": round(fl / ms / 1e9, 1)}
+                del ws
+        del q, k, v, do, dq, dk, dv
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout in the suite lines")
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -484,6 +552,7 @@ def run_ours(args):
             raise RuntimeError("a kernel reported a timeout in the sweep")
         varlen = varlen_lines(A, torch, dev, flush)
         wide = wide_lines(A, torch, dev, flush)
+        suite = suite_lines(A, torch, dev, flush)
 
     peaks, peak_src = measured_peaks()
     fwd_avg = statistics.mean(fwd_ms)
@@ -523,6 +592,7 @@ def run_ours(args):
     if not args.no_sweep:
         out["varlen_mixed_lengths"] = varlen
         out["fwd_wide_heads"] = wide
+        out["suite"] = suite
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()
         out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),
