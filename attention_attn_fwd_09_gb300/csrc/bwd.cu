@@ -288,8 +288,9 @@ struct BwdKernelArgsVL : BwdKernelArgs {
 
 // VL: packed sequences; the CTA's key block, sequence and K/V head come from its record
 // of the unit table, rows count from the sequence's start, keys past its end are masked
-// and a block that runs past the end stores dK and dV row by row.
-template <int D, bool VL>
+// and a block that runs past the end stores dK and dV row by row.  DET: the deterministic
+// dQ order (a kernel of its own, so that the atomic kernel carries none of its code).
+template <int D, bool VL, bool DET>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   //    each tile in the same iteration as block n - 1 and waits for that block's adds.
   //  Packed sequences use the shared order when deterministic; otherwise non-causal
   //  blocks start at tile n mod nqt and causal ones at their first tile.
-  const bool shared_order = a.deterministic && !a.det_rotate;
+  const bool shared_order = DET && !a.det_rotate;
   const int m_start = shared_order ? nqt - 1 : (VL ? (a.causal ? m0 : (nqt > 0 ? n % nqt : 0)) : n);
   const int m_step = shared_order ? -1 : 1;
   auto iter_head_row = [&](int it, int& bh, int& m) {
@@ -690,14 +691,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool has_col = (warp & 3) * 32 < D;        // D = 64: lanes 64-127 hold padding
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
-    bool ok = true;
-    int gphase = 0;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      int bh, m;
-      iter_head_row(it, bh, m);
-      if (!warp_wait_b(BAR(W_DQ), it & 1, wc)) { ok = false; break; }
+    // The tile's dQ from TMEM into registers; frees the columns for the next dP^T.
+    auto read_dq = [&](int it, float (&v)[128]) -> bool {
+      if (!warp_wait_b(BAR(W_DQ), it & 1, wc)) return false;
       tc_fence_after();
-      float v[128];
       if (has_col) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tdP + lane_off + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[q * 32]));
@@ -707,14 +704,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(BAR(W_DQFREE));
-      // Packed sequences: the counters of a sequence's tiles start at (q0 + 128 b) / 128.
-      int* sem = nullptr;
-      if (a.deterministic) {
+      return true;
+    };
+    // Rows are padded to whole tiles, so queries past N (or past the sequence) add into
+    // padding rows, which are never read.  Packed sequences: a sequence's rows start at
+    // q0 + 128 b of its head's rows.
+    auto add_dq = [&](int bh, int m, const float (&v)[128]) {
+      if (!has_col) return;
+      size_t arow;
+      if constexpr (VL) arow = (size_t)bh * a.rows_pad + q0 + 128 * (size_t)b + (size_t)m * 128;
+      else arow = (size_t)bh * a.nq * 128 + (size_t)m * 128;
+      red_add_rows<D>(a.dq_acc + arow * D + dcol, v, std::make_integer_sequence<int, 8>{});
+    };
+    if constexpr (!DET) {
+      for (int it = 0; it < n_iter; ++it) {
+        int bh, m;
+        iter_head_row(it, bh, m);
+        float v[128];
+        if (!read_dq(it, v)) break;
+        add_dq(bh, m, v);
+      }
+    } else {
+      int gphase = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        int bh, m;
+        iter_head_row(it, bh, m);
+        // Packed sequences: the counters of a sequence's tiles start at (q0 + 128 b) / 128.
+        int* sem;
         if constexpr (VL) sem = a.sem + (size_t)bh * a.sem_stride + (q0 + 128 * b) / 128 + m;
         else sem = a.sem + (size_t)bh * a.nq + m;
-      }
-      if (a.deterministic) {
-        // This block's turn among the tile's contributions (see the tile order above).
+        // This block's turn among the tile's contributions (see the tile order above).  The
+        // leader waits for it before the tile's dQ is ready, so the poll's round trip stays
+        // off the critical path (a turn depends only on other blocks' earlier additions).
         const int turn = a.det_rotate ? it - (it / n_m) * n_m : n;
         if (leader) {
           const unsigned long long t0 = globaltimer_ns();
@@ -727,21 +748,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
         }
-        if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) { ok = false; break; }
-      }
-      if (has_col) {
-        // Rows are padded to whole tiles, so queries past N (or past the sequence) add into
-        // padding rows, which are never read.  Packed sequences: a sequence's rows start at
-        // q0 + 128 b of its head's rows.
-        size_t arow;
-        if constexpr (VL) arow = (size_t)bh * a.rows_pad + q0 + 128 * (size_t)b + (size_t)m * 128;
-        else arow = (size_t)bh * a.nq * 128 + (size_t)m * 128;
-        float* dst = a.dq_acc + arow * D + dcol;
-        red_add_rows<D>(dst, v, std::make_integer_sequence<int, 8>{});
-      }
-      if (a.deterministic) {
-        __threadfence();                              // this thread's adds are performed
-        if (!group_sync(BAR(W_GD), gphase, wc)) { ok = false; break; }
+        float v[128];
+        if (!read_dq(it, v)) break;
+        // Every drain thread learns that the turn has come (the leader's acquire, passed on
+        // through the group barrier).
+        if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) break;
+        add_dq(bh, m, v);
+        // Release: the group barrier (its arrival releases at CTA scope) orders every
+        // drain thread's additions before the leader's gpu-scope fence, which is
+        // cumulative, and that fence before the counter's increment.
+        if (!group_sync(BAR(W_GD), gphase, wc)) break;
         if (leader) {
           __threadfence();
           atomicAdd(sem, 1);
@@ -760,7 +776,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 }  // namespace
 
-template <int D, bool VL>
+template <int D, bool VL, bool DET>
 static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) {
   // Packed sequences: N is total_q and B the number of sequences, so a head has N rows.
   const long long rows = VL ? (long long)p.Hq * p.N : (long long)p.B * p.Hq * p.N;
@@ -783,7 +799,7 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   if (e != cudaSuccess) return e;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   {
-    auto kern = attn_bwd_kernel<D, VL>;
+    auto kern = attn_bwd_kernel<D, VL, DET>;
     constexpr uint32_t smem = BwdCfg<D>::SMEM;
     static std::once_flag flags[64];
     static cudaError_t attr_err[64];
@@ -823,14 +839,19 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   }
 }
 
+template <int D, bool VL>
+static cudaError_t launch_bwd_det(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream) {
+  return p.deterministic ? launch_bwd_t<D, VL, true>(maps, p, stream) : launch_bwd_t<D, VL, false>(maps, p, stream);
+}
+
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream) {
   if (p.varlen) {
-    if (p.D == 64) return launch_bwd_t<64, true>(maps, p, stream);
-    if (p.D == 128) return launch_bwd_t<128, true>(maps, p, stream);
+    if (p.D == 64) return launch_bwd_det<64, true>(maps, p, stream);
+    if (p.D == 128) return launch_bwd_det<128, true>(maps, p, stream);
     return cudaErrorNotSupported;
   }
-  if (p.D == 64) return launch_bwd_t<64, false>(maps, p, stream);
-  if (p.D == 128) return launch_bwd_t<128, false>(maps, p, stream);
+  if (p.D == 64) return launch_bwd_det<64, false>(maps, p, stream);
+  if (p.D == 128) return launch_bwd_det<128, false>(maps, p, stream);
   return cudaErrorNotSupported;
 }
 
