@@ -355,21 +355,23 @@ int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse
 
 // Packed variable-length sequences.  The unit table's size is bounded from the packed
 // length alone: sum_b ceil(nq_b / 128) <= floor(total_q / 128) + B tiles per head.
-static long long varlen_cap(int B, int Hq, int Hkv, int total_q) {
+static long long varlen_cap(int B, int Hq, int Hkv, int total_q, int d) {
   const int g = Hq / Hkv;
   const bool pair = g >= 2 && g % 2 == 0;
   const long long tiles = (long long)total_q / 128 + B;
+  if (d > 128) return tiles * Hq;   // one tile per record (the one-tile kernel)
   return pair ? tiles * (Hq / 2) : ((tiles + B + 1) / 2) * Hq;
 }
 static constexpr size_t kVarlenHeader = 256;   // [0] records, [1] offsets invalid
 
 size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 || (d != 64 && d != 128)) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 ||
+      (d != 64 && d != 128 && d != 192 && d != 256)) {
     set_last_error("attn_fwd_varlen_workspace_size: invalid sizes");
     return (size_t)-1;
   }
   if (B == 0 || total_q == 0) return 0;
-  return kVarlenHeader + (size_t)varlen_cap(B, Hq, Hkv, total_q) * sizeof(int4);
+  return kVarlenHeader + (size_t)varlen_cap(B, Hq, Hkv, total_q, d) * sizeof(int4);
 }
 
 int attn_set_fwd_one_tile(int enable) {
@@ -385,7 +387,7 @@ int attn_set_varlen_order(int longest_first) {
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
                     const int* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int d, int causal,
                     float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_shape(B, Hq, Hkv, total_q, d, scale);
+  int rc = check_shape(B, Hq, Hkv, total_q, d, scale, true);
   if (rc != ATTN_OK) return rc;
   if (total_k < 0) return fail(ATTN_ERR_INVALID_ARG, "total_k=%d must be >= 0", total_k);
   if (total_q > 0x7fffff00 || total_k > 0x7fffff00)
@@ -399,7 +401,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
     return fail(ATTN_ERR_MISALIGNED, "q, k, v, o and lse must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u)
     return fail(ATTN_ERR_MISALIGNED, "cu_seqlens_q and cu_seqlens_k must be 4-byte aligned");
-  const long long cap = varlen_cap(B, Hq, Hkv, total_q);
+  const long long cap = varlen_cap(B, Hq, Hkv, total_q, d);
   const size_t need = kVarlenHeader + (size_t)cap * sizeof(int4);
   if (!workspace || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
@@ -439,8 +441,10 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   VarlenSched sc{};
   sc.cu_q = cu_seqlens_q;
   sc.cu_k = cu_seqlens_k;
+  const bool wide = d > 128;        // one query tile per CTA (the one-tile kernel)
   sc.backward = 0;
-  sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = p.pair_heads; sc.causal = p.causal;
+  sc.single = wide ? 1 : 0;
+  sc.B = B; sc.Hq = Hq; sc.Hkv = Hkv; sc.pair_heads = wide ? 0 : p.pair_heads; sc.causal = p.causal;
   sc.total_q = total_q; sc.total_k = total_k;
   sc.nbins = (int)std::min<long long>((total_k + 127LL) / 128 + 1, 32768LL);   // classes: a sequence's key blocks
   sc.cap = (int)cap;
@@ -451,7 +455,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_varlen_schedule(sc, st);
   if (e != cudaSuccess) return cuda_fail(e, "unit table launch");
-  e = launch_fwd(maps, p, d, 0, (int)cap, st);
+  e = wide ? launch_fwd_wide(maps, p, d, (int)cap, st) : launch_fwd(maps, p, d, 0, (int)cap, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return post_launch(s, st);
 }

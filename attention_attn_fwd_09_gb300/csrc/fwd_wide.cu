@@ -100,9 +100,12 @@ __device__ __forceinline__ bool item_at(int pos, int n, int& j) {
 }
 
 // CTA -> (b * Hq + hq, 128-row block).  Causal grids run the longest rows first; others
-// run the row blocks of a head back to back (its K and V stay hot in L2).
+// run the row blocks of a head back to back (its K and V stay hot in L2).  The sequence
+// fields (first query row qs, one past the last qend, first key row krow0, keys nk,
+// nk - nq = koff) are constants of the launch except for packed sequences.
 struct WideTile {
   int n, row0, bh, bkv;
+  int qs, qend, krow0, nk, koff;
 };
 __device__ __forceinline__ WideTile map_wide(const FwdParams& p, int cta) {
   WideTile T;
@@ -119,10 +122,27 @@ __device__ __forceinline__ WideTile map_wide(const FwdParams& p, int cta) {
   const int b = T.bh / p.Hq, hq = T.bh % p.Hq;
   T.bkv = b * p.Hkv + hq / p.g;
   T.n = p.causal ? (min(T.row0 + 127, p.N - 1) + p.koff) / 128 + 1 : p.n_kvblk;
+  T.qs = 0; T.qend = p.N; T.krow0 = 0; T.nk = p.Nk; T.koff = p.koff;
   return T;
 }
 
-template <int D>
+// Packed sequences: the CTA's record of the unit table (varlen.cu, one tile per record)
+// names the sequence, the query head and the tile's first row within the sequence.
+__device__ __forceinline__ WideTile map_wide_varlen(const FwdParams& p, const int4 u) {
+  WideTile T;
+  const int b = u.x, hq = u.y & 0xffff, r0 = u.z;
+  const int q0 = p.cu_q[b], nq = p.cu_q[b + 1] - q0;
+  const int k0 = p.cu_k[b], nk = p.cu_k[b + 1] - k0;
+  T.qs = q0; T.qend = q0 + nq; T.krow0 = k0; T.nk = nk; T.koff = nk - nq;
+  T.row0 = q0 + r0;
+  T.bh = hq;
+  T.bkv = hq / p.g;
+  T.n = p.causal ? (min(r0 + 127, nq - 1) + T.koff) / 128 + 1 : (nk + 127) / 128;
+  return T;
+}
+
+// VL: packed variable-length sequences (d = 192, 256): one unit-table record per CTA.
+template <int D, bool VL>
 __global__ void __launch_bounds__(kWideThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -145,7 +165,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int wg = warp >> 2;
-  const WideTile T = map_wide(p, blockIdx.x);
+  WideTile T;
+  if constexpr (VL) {
+    // CTAs past the table's records have no work: they leave before touching barriers or
+    // tensor memory.
+    if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
+    T = map_wide_varlen(p, p.vl_units[blockIdx.x]);
+  } else {
+    T = map_wide(p, blockIdx.x);
+  }
   const int n = T.n;
   WaitCtl wc{p.wait_ns, p.status, abort_flag};
 
@@ -211,7 +239,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_arrive_expect_tx(BAR(V_FULL + slot), C::TILE);
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, T.bkv,
+          tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, T.krow0 + j * 128, T.bkv,
                       BAR(V_FULL + slot));
       }
       if (!ok) {
@@ -301,9 +329,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       reg_fence_w(u);
       float* s = reinterpret_cast<float*>(u);
       const int kb = j * 128 + h * 64;
-      const bool need_mask = (kb + 63 >= p.Nk) || (p.causal && kb + 63 > T.row0 + p.koff);
+      const bool need_mask = (kb + 63 >= T.nk) || (p.causal && kb + 63 > T.row0 - T.qs + T.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(grow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;   // last visible column
+        const int lim = (p.causal ? min(grow - T.qs + T.koff, T.nk - 1) : T.nk - 1) - kb;   // last visible column
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -386,10 +414,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tmem_wait_ld();
       reg_fence_w(u);
       float* s = reinterpret_cast<float*>(u);
+      // Packed sequences: keys count from the sequence's start; those past its end (the
+      // next sequence's) are masked like those past the tensor's end.
       const int kb = j * 128;
-      const bool need_mask = (kb + 127 >= p.Nk) || (p.causal && kb + 127 > T.row0 + p.koff);
+      const bool need_mask = (kb + 127 >= T.nk) || (p.causal && kb + 127 > T.row0 - T.qs + T.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(grow + p.koff, p.Nk - 1) : p.Nk - 1) - kb;   // last visible column
+        const int lim = (p.causal ? min(grow - T.qs + T.koff, T.nk - 1) : T.nk - 1) - kb;   // last visible column
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -496,6 +526,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const float lrow = C::SPLIT ? l_fin[row] + l_fin[128 + row] : l_fin[row];
       const float inv = 1.f / (C::SPLIT ? lq_fin[row] + lq_fin[128 + row] : lq_fin[row]);
       uint8_t* stage = smem + C::OFF_Q;
+      const int grow = T.row0 + row;
+      // Packed sequences: a tile that runs past its sequence's last row is written row by
+      // row (a TMA store would overwrite the next sequence's first rows).
+      const bool direct = VL && T.row0 + 128 > T.qend;
+      uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) + ((size_t)T.bh * p.N + grow) * D;
       uint32_t r[32];
 #pragma unroll 1
       for (int q = 0; q < C::OCOLS / 32; ++q) {
@@ -507,6 +542,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
         const int col = half * C::OCOLS + q * 32;
+        if (direct) {
+          if (grow < T.qend) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(orow + col + u * 8) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+          continue;
+        }
         const int box = col / 64, j0 = (col % 64) / 8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -514,16 +558,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           *reinterpret_cast<uint4*>(stage + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      const int grow = T.row0 + row;
-      if (half == 0 && grow < p.N)
+      if (half == 0 && grow < T.qend)
         p.lse[(size_t)T.bh * p.N + grow] = (m_fin[row] + __log2f(lrow)) * kLn2;
-      fence_proxy_async_smem();
-      mbar_arrive(BAR(V_EPI));
-      if (warp == 4 * C::FIRST_CORR_WG && lane == 0 && mbar_wait(BAR(V_EPI), 0, wc)) {
-        for (int c = 0; c < C::NCH; ++c)
-          tma_store_3d(&tm_o, sbase + C::OFF_Q + c * C::CHUNK, c * 64, T.row0, T.bh);
-        tma_store_commit();
-        tma_store_wait_all();
+      if (!direct) {
+        fence_proxy_async_smem();
+        mbar_arrive(BAR(V_EPI));
+        if (warp == 4 * C::FIRST_CORR_WG && lane == 0 && mbar_wait(BAR(V_EPI), 0, wc)) {
+          for (int c = 0; c < C::NCH; ++c)
+            tma_store_3d(&tm_o, sbase + C::OFF_Q + c * C::CHUNK, c * 64, T.row0, T.bh);
+          tma_store_commit();
+          tma_store_wait_all();
+        }
       }
     }
   }
@@ -536,9 +581,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool VL>
 cudaError_t launch_wide_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
-  auto kern = attn_fwd_wide_kernel<D>;
+  auto kern = attn_fwd_wide_kernel<D, VL>;
   constexpr uint32_t smem = WideCfg<D>::SMEM;
   static std::once_flag flags[64];
   static cudaError_t attr_err[64];
@@ -556,9 +601,14 @@ cudaError_t launch_wide_t(const FwdMaps& m, const FwdParams& p, int grid, cudaSt
 }  // namespace
 
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t s) {
-  if (D == 128) return launch_wide_t<128>(maps, p, grid, s);
-  if (D == 192) return launch_wide_t<192>(maps, p, grid, s);
-  if (D == 256) return launch_wide_t<256>(maps, p, grid, s);
+  if (p.pack == 2) {   // packed sequences (d = 192, 256)
+    if (D == 192) return launch_wide_t<192, true>(maps, p, grid, s);
+    if (D == 256) return launch_wide_t<256, true>(maps, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
+  if (D == 128) return launch_wide_t<128, false>(maps, p, grid, s);
+  if (D == 192) return launch_wide_t<192, false>(maps, p, grid, s);
+  if (D == 256) return launch_wide_t<256, false>(maps, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

@@ -66,6 +66,7 @@ struct VarlenSched {
   const int* cu_q;
   const int* cu_k;
   int backward;            // 0: forward records; 1: backward records {b, hkv, key block, 0}
+  int single;              // forward: one query tile per record (the one-tile kernel, d > 128)
   int B, Hq, Hkv, pair_heads, causal, total_q, total_k;
   int nbins;               // work classes (a sequence's key blocks, clamped to nbins - 1)
   int cap;                 // records the table can hold

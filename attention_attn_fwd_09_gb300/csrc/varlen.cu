@@ -18,7 +18,9 @@
 // sequence b (query heads hq0 and hq1; r1 < 0 when the sequence's last tile has no
 // partner).  The pairing is the ordinary forward's: two query heads of one K/V group on
 // the same rows when the group size is even, otherwise two consecutive row tiles of one
-// head.  Backward records: {b, hkv, n, 0}: key block n of sequence b and K/V head hkv.
+// head; with `single` (the one-tile kernel of wide heads) a record is one tile of one
+// head, {b, hq | hq << 16, r0, -1}.  Backward records: {b, hkv, n, 0}: key block n of
+// sequence b and K/V head hkv.
 #include <cstdint>
 #include <mutex>
 
@@ -42,11 +44,12 @@ template <int PHASE>
 __device__ void visit_slots(const VarlenSched& s, int* hist) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = s.backward ? s.Hkv : (s.pair_heads ? s.Hq / 2 : s.Hq);
+  const bool one_row = s.single || s.pair_heads;   // a slot is one row tile
   for (int b = warp; b < s.B; b += kSchedThreads / 32) {
     const int q0 = s.cu_q[b], nq = s.cu_q[b + 1] - q0;
     const int nk = s.cu_k[b + 1] - s.cu_k[b];
     const int tiles = (nq + 127) / 128;
-    const int slots = s.backward ? (nk + 127) / 128 : (s.pair_heads ? tiles : (tiles + 1) / 2);
+    const int slots = s.backward ? (nk + 127) / 128 : (one_row ? tiles : (tiles + 1) / 2);
     const int work = s.lpt ? min((nk + 127) / 128, s.nbins - 1) : 0;
     for (int base = 0; base < slots; base += 32) {
       const int i = base + lane;
@@ -55,6 +58,8 @@ __device__ void visit_slots(const VarlenSched& s, int* hist) {
       int r0 = 0, r1 = -1;
       if (s.backward) {
         r0 = sl;
+      } else if (s.single) {
+        r0 = sl * 128;
       } else {
         r0 = s.pair_heads ? sl * 128 : sl * 256;
         r1 = s.pair_heads ? r0 : (r0 + 128 < nq ? r0 + 128 : -1);

@@ -61,7 +61,7 @@ typedef enum {
  *   d:      64, 128, 192 or 256.  For 192 and 256 (up to the 256 of "Hotelren FA4
  *           summary" section 6.2, item 1) the two tiles' accumulators do not fit tensor
  *           memory, so a CTA takes one query tile and overlaps the softmax of one key
- *           block with the products of the next.  Backward and packed sequences: 64, 128.
+ *           block with the products of the next.  The backward: 64 and 128.
  *   causal: 0 or 1 (key j visible to query i only if j <= i)
  *   scale:  softmax scale applied to Q K^T
  */
@@ -111,6 +111,7 @@ size_t attn_fwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d)
  *       aligned, owned by the caller, contents on entry irrelevant (it receives the
  *       order in which the tiles run, built on the device from the offsets).
  *   other arguments and ownership as attn_fwd.
+ * Head dims as attn_fwd (64, 128, 192, 256).
  * Errors as attn_fwd, plus ATTN_ERR_WORKSPACE, ATTN_ERR_INVALID_ARG when total_k = 0 <
  * total_q, and ATTN_ERR_UNSUPPORTED for Hq > 65535.  The offsets are checked on the
  * device: if they break a rule above, nothing is written to o and lse and the device

@@ -135,7 +135,9 @@ def test_fwd_varlen_argument_errors(lib):
     def call(B=2, Hq=4, Hkv=4, tq=300, tk=300, d=64, causal=0, cu=FAKE, ws=FAKE, ws_bytes=1 << 20):
         return lib.attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, cu, B, Hq, Hkv, tq, tk, d, causal, 0.1,
                                    ws, ws_bytes, None)
-    assert call(d=96) == -2 and call(d=256) == -2
+    assert call(d=96) == -2
+    # wide heads: one tile per record, floor(300/128) + 2 = 4 tiles per head at most
+    assert lib.attn_fwd_varlen_workspace_size(2, 4, 4, 300, 256) == 256 + 4 * 4 * 16
     assert call(tk=0) == -1 and b"no keys" in lib.attn_last_error()
     assert call(Hq=70000, Hkv=70000) == -2
     assert call(cu=ctypes.c_void_p(0x10002)) == -3

@@ -30,6 +30,9 @@ CASES = {  # name: (lens_q, extra keys per sequence or None for nk = nq, Hq, Hkv
     "mqa_d64": ([900, 17, 256, 511], None, 4, 1, 64),
     "longer_keys_d128": ([100, 1, 300, 128, 40], [29, 700, 1, 128, 0], 4, 2, 128),
     "single_seq_d128": ([1500], None, 2, 2, 128),
+    # wide heads: the one-tile kernel, one table record per tile
+    "wide_d256": ([300, 1, 640, 129], None, 4, 2, 256),
+    "wide_d192_longer_keys": ([100, 7, 300, 0], [229, 7, 900, 3], 2, 1, 192),
 }
 
 
@@ -60,7 +63,8 @@ def test_varlen_matches_oracle(A, name, causal):
     check_fwd(o.float().cpu().numpy(), lse.cpu().numpy(), O, L, f"{name} causal={causal}")
 
 
-@pytest.mark.parametrize("name", ["ragged_mha_d128", "gqa_pairs_d128", "longer_keys_d128", "odd_group_d128"])
+@pytest.mark.parametrize("name", ["ragged_mha_d128", "gqa_pairs_d128", "longer_keys_d128", "odd_group_d128",
+                                  "wide_d256", "wide_d192_longer_keys"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_equals_each_sequence_alone(A, name, causal):
     # Every tile does the same arithmetic as in a call on its sequence alone: keys past the
