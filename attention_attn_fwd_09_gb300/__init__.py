@@ -40,6 +40,8 @@ _lib.attn_bwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i,
 _lib.attn_bwd_varlen.restype = _i
 _lib.attn_bwd_varlen_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.attn_bwd_varlen_workspace_size.restype = _sz
+_lib.attn_set_fwd_persistent.argtypes = [_i]
+_lib.attn_set_fwd_persistent.restype = _i
 _lib.attn_set_fwd_one_tile.argtypes = [_i]
 _lib.attn_set_fwd_one_tile.restype = _i
 _lib.attn_set_varlen_order.argtypes = [_i]
@@ -252,6 +254,11 @@ def attn_bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, causal: boo
                                 int(bool(causal)), float(scale), int(bool(deterministic)), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return dq, dk, dv
+
+
+def attn_set_fwd_persistent(enable: bool):
+    """d = 64/128 forward: one CTA per SM walking the work list (True) or one per unit."""
+    _check(_lib.attn_set_fwd_persistent(int(bool(enable))))
 
 
 def attn_set_fwd_one_tile(enable: bool):

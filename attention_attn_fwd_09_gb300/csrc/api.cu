@@ -47,6 +47,7 @@ std::atomic<int> g_count_rescales{0};
 std::atomic<int> g_test_skip_kv{0};
 std::atomic<int> g_varlen_lpt{1};
 std::atomic<int> g_one_tile_d128{0};
+std::atomic<int> g_persistent{0};
 
 struct DevSyms {
   int* status = nullptr;
@@ -325,8 +326,17 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   }
   if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wide ? launch_fwd_wide(maps, p, d, (int)grid, st)
-                        : launch_fwd(maps, p, d, pack ? 0 : g_poly.load(), (int)grid, st);
+  // Persistent two-tile kernel (fwd_persist.cu): one CTA per SM walking the same work list.
+  const bool persist = !wide && !pack && g_persistent.load() && g_poly.load() == 0;
+  cudaError_t e;
+  if (persist) {
+    p.o_ptr = o;
+    const long long entries = grid;
+    const long long pgrid = std::min<long long>(entries, std::max(1, s->sms));
+    e = launch_fwd_persistent(maps, p, d, (int)pgrid, (int)entries, st);
+  } else {
+    e = wide ? launch_fwd_wide(maps, p, d, (int)grid, st) : launch_fwd(maps, p, d, pack ? 0 : g_poly.load(), (int)grid, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   if (pack && (e = launch_fwd_merge(p, d, o, st)) != cudaSuccess) return cuda_fail(e, "forward merge launch");
   return post_launch(s, st);
@@ -372,6 +382,11 @@ size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d
   }
   if (B == 0 || total_q == 0) return 0;
   return kVarlenHeader + (size_t)varlen_cap(B, Hq, Hkv, total_q, d) * sizeof(int4);
+}
+
+int attn_set_fwd_persistent(int enable) {
+  g_persistent.store(enable ? 1 : 0);
+  return ATTN_OK;
 }
 
 int attn_set_fwd_one_tile(int enable) {

@@ -77,6 +77,11 @@ struct VarlenSched {
 };
 cudaError_t launch_varlen_schedule(const VarlenSched& s, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
+// Persistent two-tile forward (fwd_persist.cu), d = 64 or 128, ordinary mode, MUFU
+// exponentials: grid CTAs walk entries 0 .. n_entries - 1 of the work list (units below
+// p.split_from whole, then one-tile halves) in steps of grid; O is written through p.o_ptr.
+cudaError_t launch_fwd_persistent(const FwdMaps& maps, const FwdParams& p, int D, int grid, int n_entries,
+                                  cudaStream_t stream);
 // One-tile forward (fwd_wide.cu) for d = 128, 192 or 256: one 128-row query tile per CTA,
 // grid = B * Hq * ceil(N / 128); same parameters as launch_fwd (ordinary mode only).
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t stream);

@@ -157,6 +157,15 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
 size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
 
 /*
+ * Persistent forward for d = 64 and 128 (ordinary tiling): 1 = one CTA per SM walks the
+ * work list, loading the next unit's tiles and starting its products while the current
+ * unit ends (fwd_persist.cu); 0 = one CTA per unit (fwd.cu).  Same results bit for bit.
+ * Grouped decode, packed sequences and the exponential-split knob keep the per-unit
+ * kernel.  A tuning knob, process-wide.
+ */
+int attn_set_fwd_persistent(int enable);
+
+/*
  * Which forward kernel serves d = 128: 0 = two query tiles per CTA (fwd.cu), 1 = one
  * query tile per CTA with the softmax of each key block split over two warpgroups
  * (fwd_wide.cu, the kernel that always serves d = 192 and 256).  Same results up to the
