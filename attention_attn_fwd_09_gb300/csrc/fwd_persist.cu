@@ -18,11 +18,13 @@
 //     buffer, which the next unit's Q is already filling) while the tensor core computes
 //     the next unit's first S; the next unit's first PV waits for it through the P-ready
 //     barrier, which the correction group joins only after its epilogue.
-// Measured on GB300 it is slower than the per-unit kernel except for the shortest units
-// (N = 512: +4 %; N = 2048: -7 %; N = 16384: -9 %; causal down to -16 %), so it is opt-in
-// (attn_set_fwd_persistent).  Its register split leaves the softmax 184 registers instead
-// of 192 (the MMA warp needs more than 56 here), and a static share of causal units is
-// less even than the hardware's CTA-by-CTA dispatch.
+// Measured on GB300 it beats the per-unit kernel only for the shortest units (N = 512:
+// +7 %, N = 1024: +1 %) and trails it from N = 2048 on (-4 to -8 %; causal -10 to -15 %,
+// where a static share of units is also less even than the hardware's CTA-by-CTA
+// dispatch), so it is opt-in (attn_set_fwd_persistent).  Same DRAM traffic and L2 hit
+// rate as the per-unit kernel, but less tensor-pipe activity in the steady state, for a
+// reason not found: neither the register split (the per-unit kernel runs the same one)
+// nor local memory (none) nor the Q loader's polling (paced) explains it.
 #include <cstdint>
 #include <mutex>
 
@@ -233,9 +235,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int e = e0; e < n_entries; e += estep) {
         const PTiles T = pentry(p, e);
         if (max(T.n[0], T.n[1]) == 0) continue;
-        if (u > 0 && !mbar_wait(BAR(P_QFREE), (u - 1) & 1, wc)) {
-          ok = false;
-          break;
+        // The wait spans a whole unit and is not latency-critical at the microsecond
+        // scale: poll with pauses, so as not to take issue slots from the softmax and
+        // correction warps that share this warp's scheduler.
+        if (u > 0) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (!mbar_try_wait(BAR(P_QFREE), (u - 1) & 1)) {
+            if (*abort_flag) { ok = false; break; }
+            if (globaltimer_ns() - t0 > p.wait_ns) {
+              *abort_flag = 1;
+              atomicExch(p.status, DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+            __nanosleep(256);
+          }
+          if (!ok) break;
         }
         mbar_arrive_expect_tx(BAR(P_Q), (T.n[0] > 0 ? C::TILE : 0) + (T.n[1] > 0 ? C::TILE : 0));
 #pragma unroll
@@ -259,27 +274,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // (the previous unit's last block when G opens a unit) then S of block G; a commit
       // then releases K_G and V_(G-1).
       int G = 0, u = 0;
-      int pv_cnt[2] = {0, 0};     // PV products issued per tile (P-ready phases)
-      PTiles prev;
-      int prev_nmax = 0;
-      prev.n[0] = prev.n[1] = 0;
+      // PV products issued per tile (their P-ready phases); scalars, so that nothing of
+      // the issuing thread's state lives in local memory.
+      int pvc0 = 0, pvc1 = 0;
+      int prev_n0 = 0, prev_n1 = 0, prev_nmax = 0;
       bool ok = true;
       const uint32_t qb = sbase + C::OFF_Q;
       // PV_t of the block at ring position vpos: O_t (+)= P_t V; `last` marks the tile's
       // last block of its unit (its completion is what the epilogue waits for).
-      auto issue_pv = [&](int t, int vpos, bool first, bool last) -> bool {
-        if (!mbar_wait(BAR(P_PFULL + t), pv_cnt[t] & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sbase + C::OFF_RING + (vpos % C::NS) * C::TILE;
-        const uint32_t tS = tmem + uint32_t(t * 128), tO = tmem + 256u + uint32_t(t * D);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
-                 (!first || kk > 0) ? 1u : 0u);
-        ++pv_cnt[t];
-        if (last) mma_commit(BAR(P_OFULL + t));
-        return true;
-      };
+#define PV_ISSUE(t, pvc, vpos, first, last)                                                              \
+  if (ok) {                                                                                               \
+    if (!mbar_wait(BAR(P_PFULL + (t)), (pvc) & 1, wc)) {                                                  \
+      ok = false;                                                                                         \
+    } else {                                                                                              \
+      tc_fence_after();                                                                                   \
+      const uint32_t vbase_ = sbase + C::OFF_RING + ((vpos) % C::NS) * C::TILE;                          \
+      const uint32_t tS_ = tmem + uint32_t((t) * 128), tO_ = tmem + 256u + uint32_t((t) * D);            \
+      _Pragma("unroll") for (int kk = 0; kk < 8; ++kk)                                                    \
+        mma_ts(tO_, tS_ + kk * 8, sdesc_sw128(vbase_ + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,          \
+               (!(first) || kk > 0) ? 1u : 0u);                                                           \
+      ++(pvc);                                                                                            \
+      if (last) mma_commit(BAR(P_OFULL + (t)));                                                           \
+    }                                                                                                     \
+  }
       for (int e = e0; e < n_entries && ok; e += estep) {
         const PTiles T = pentry(p, e);
         const int nmax = max(T.n[0], T.n[1]);
@@ -290,37 +307,53 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (G > 0 && !mbar_wait(BAR(P_FULL + vpos % C::NS), (vpos / C::NS) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kbase = sbase + C::OFF_RING + (kpos % C::NS) * C::TILE;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok) break;
-            // PV of the previous block of this tile, if there is one.
+          // Tile 0: PV of its previous block (if any), the unit's Q (before its first S;
+          // tile 0 always has one at j = 0), S of block j.  Then the same for tile 1.
+          do {
             if (j == 0) {
-              if (prev.n[t] > 0 && prev.n[t] == prev_nmax && !issue_pv(t, vpos, prev.n[t] == 1, true)) { ok = false; break; }
-            } else if (j - 1 < T.n[t]) {
-              if (!issue_pv(t, vpos, j == 1, j == T.n[t])) { ok = false; break; }
+              if (prev_n0 > 0 && prev_n0 == prev_nmax) PV_ISSUE(0, pvc0, vpos, prev_n0 == 1, true);
+            } else if (j - 1 < T.n[0]) {
+              PV_ISSUE(0, pvc0, vpos, j == 1, j == T.n[0]);
             }
-            // The unit's Q tiles, before its first S (tile 0 always has one at j = 0).
-            if (j == 0 && t == 0) {
+            if (!ok) break;
+            if (j == 0) {
               if (!mbar_wait(BAR(P_Q), u & 1, wc)) { ok = false; break; }
               tc_fence_after();
             }
-            if (j < T.n[t]) {
-              const uint32_t tS = tmem + uint32_t(t * 128);
-              const uint32_t qbase = qb + t * C::TILE;
+            if (j < T.n[0]) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                mma_ss(tS, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
+                mma_ss(tmem, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
                        kk > 0 ? 1u : 0u);
               }
-              mma_commit(BAR(P_SFULL + t));
+              mma_commit(BAR(P_SFULL + 0));
             }
-          }
+          } while (0);
+          if (!ok) break;
+          do {
+            if (j == 0) {
+              if (prev_n1 > 0 && prev_n1 == prev_nmax) PV_ISSUE(1, pvc1, vpos, prev_n1 == 1, true);
+            } else if (j - 1 < T.n[1]) {
+              PV_ISSUE(1, pvc1, vpos, j == 1, j == T.n[1]);
+            }
+            if (!ok) break;
+            if (j < T.n[1]) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+                mma_ss(tmem + 128u, sdesc_sw128(qb + C::TILE + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                       C::IDESC_QK, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(BAR(P_SFULL + 1));
+            }
+          } while (0);
           if (!ok) break;
           if (j == nmax - 1) mma_commit(BAR(P_QFREE));   // every S of the unit issued before this
           mma_commit(BAR(P_REL + (G & 1)));
         }
-        prev = T;
+        prev_n0 = T.n[0];
+        prev_n1 = T.n[1];
         prev_nmax = nmax;
         ++u;
       }
@@ -329,10 +362,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int vpos = 2 * G - 1;
         if (mbar_wait(BAR(P_FULL + vpos % C::NS), (vpos / C::NS) & 1, wc)) {
           tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t)
-            if (prev.n[t] > 0 && prev.n[t] == prev_nmax && !issue_pv(t, vpos, prev.n[t] == 1, true)) ok = false;
+          do {
+            if (prev_n0 > 0 && prev_n0 == prev_nmax) PV_ISSUE(0, pvc0, vpos, prev_n0 == 1, true);
+            if (prev_n1 > 0 && prev_n1 == prev_nmax) PV_ISSUE(1, pvc1, vpos, prev_n1 == 1, true);
+          } while (0);
         }
       }
+#undef PV_ISSUE
       mma_commit(BAR(P_DONE));
       const unsigned long long t0 = globaltimer_ns();
       while (!mbar_try_wait(BAR(P_DONE), 0) && globaltimer_ns() - t0 < p.wait_ns) {
@@ -350,9 +386,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     for (int e = e0; e < n_entries && ok; e += estep) {
       const PTiles T = pentry(p, e);
-      const int n_t = T.n[t];
+      // Select, not index: t is not a compile-time constant, and an indexed struct would
+      // live in local memory.
+      const int n_t = t ? T.n[1] : T.n[0];
       if (n_t == 0) continue;
-      const int row0_t = T.row0[t];
+      const int row0_t = t ? T.row0[1] : T.row0[0];
       const int grow = row0_t + row;
       float m = -INFINITY, l = 0.f, lq = 0.f;
       for (int j = 0; j < n_t; ++j, ++cnt) {
