@@ -108,6 +108,33 @@ def _dev_bf16(name, t, shape):
                          f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
 
 
+def _dev_f32(name, t, shape):
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected a contiguous CUDA fp32 tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+def _bwd_tensors(q, k, v, o, lse, do, dq, dk, dv):
+    """Checks the backward's inputs and outputs ([B,Hq,N,d] / [B,Hkv,N,d] bf16, lse [B,Hq,N]
+    fp32, all on one device) and allocates the outputs not given."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    for name, t, shp in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
+                         ("o", o, (B, Hq, N, d)), ("do", do, (B, Hq, N, d))):
+        _dev_bf16(name, t, shp)
+    _dev_f32("lse", lse, (B, Hq, N))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _dev_bf16("dq", dq, (B, Hq, N, d))
+    _dev_bf16("dk", dk, (B, Hkv, N, d))
+    _dev_bf16("dv", dv, (B, Hkv, N, d))
+    for name, t in (("k", k), ("v", v), ("o", o), ("lse", lse), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+    return B, Hq, Hkv, N, d, dq, dk, dv
+
+
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
     """O, LSE = attention(q, k, v).  q [B,Hq,N,d], k/v [B,Hkv,N,d] CUDA bf16.
 
@@ -280,16 +307,9 @@ def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, d: int, determini
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, deterministic: bool = False,
              dq=None, dk=None, dv=None, workspace=None, stream=None):
     """dQ, dK, dV of attention given the forward's o, lse and the upstream gradient do."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    for name, t, shp in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
-                         ("o", o, (B, Hq, N, d)), ("do", do, (B, Hq, N, d))):
-        _dev_bf16(name, t, shp)
+    B, Hq, Hkv, N, d, dq, dk, dv = _bwd_tensors(q, k, v, o, lse, do, dq, dk, dv)
     if scale is None:
         scale = d ** -0.5
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d, deterministic)
     if workspace is None:
         workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=q.device)
@@ -304,16 +324,9 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, causal: bool = False, scale: float | N
     """attn_bwd without a workspace, for callers that cannot allocate device memory on
     the call path; the library's own fixed 64 MiB array serves as the workspace (sizes
     needing more are rejected).  Overlapping calls on different streams race on it."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    for name, t, shp in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
-                         ("o", o, (B, Hq, N, d)), ("do", do, (B, Hq, N, d))):
-        _dev_bf16(name, t, shp)
+    B, Hq, Hkv, N, d, dq, dk, dv = _bwd_tensors(q, k, v, o, lse, do, dq, dk, dv)
     if scale is None:
         scale = d ** -0.5
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
     _check(_lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                                  int(bool(deterministic)), _stream(stream)))

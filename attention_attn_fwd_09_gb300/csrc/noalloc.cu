@@ -9,9 +9,9 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the library holds
 // kNoallocScratchBytes of it until the process exits.  In host code its name is only a
-// host-side stand-in, so its device address is looked up once per device with
-// cudaGetSymbolAddress (on the first call made on that device) and passed on as an
-// ordinary pointer.  All calls share the one array: calls that overlap on the GPU (for
+// host-side stand-in, so its device address is looked up per device with
+// cudaGetSymbolAddress (on the first call made on that device, again on the next call if
+// that lookup failed) and passed on as an ordinary pointer.  All calls share the one array: calls that overlap on the GPU (for
 // example on two streams) race on it.  It keeps the previous call's contents; the
 // backward's own first kernel clears everything that must start at zero.
 #include <cstdio>
@@ -31,9 +31,11 @@ constexpr size_t kNoallocScratchBytes = size_t(64) << 20;  // 64 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
+// The array's device address per device, once looked up.  Only a successful lookup is
+// kept: a call whose lookup failed (a sticky error left by an earlier launch, or a first
+// call made during stream capture) reports it, and the next call tries again.
 void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu[kMaxDevices];
 
 }  // namespace
 
@@ -60,20 +62,24 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
     attn::set_last_error(msg);
     return ATTN_ERR_CUDA;
   }
-  // Once per device, with that device current: the array's device address.
-  std::call_once(g_scratch_once[dev], [dev] {
-    void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) {
-    snprintf(msg, sizeof msg, "attn_bwd_noalloc: cudaGetSymbolAddress failed (%s)",
-             cudaGetErrorString(g_scratch_err[dev]));
-    attn::set_last_error(msg);
-    return ATTN_ERR_CUDA;
+  // With that device current: the array's device address, looked up until it succeeds.
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu[dev]);
+    if (g_scratch_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        snprintf(msg, sizeof msg, "attn_bwd_noalloc: cudaGetSymbolAddress failed (%s)", cudaGetErrorString(e));
+        attn::set_last_error(msg);
+        return ATTN_ERR_CUDA;
+      }
+      g_scratch_ptr[dev] = p;
+    }
+    scratch = g_scratch_ptr[dev];
   }
-  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, deterministic,
-                  g_scratch_ptr[dev], kNoallocScratchBytes, stream);
+  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, deterministic, scratch,
+                  kNoallocScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -52,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--profile", action="store_true",
                     help="short run for a profiler: warm-up plus the timed steps only (no e2e, sweep or CPU leg)")
+    ap.add_argument("--case", default=None,
+                    help="run one kernel configuration (see CASES) --warmup + --steps times and print its "
+                         "median time: a small, single-kernel target for a profiler")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -382,6 +385,163 @@ def suite_lines(A, torch, dev, flush):
     return res
 
 
+def decode_lines(A, torch, dev, flush):
+    """Decoding against a key/value cache (attn_fwd_kv): B=8, Hq=32, Hkv=8, Nk=8192, d=128,
+    causal, Nq new queries per head.  The forward reads the whole cache once, so the line
+    is reported as cache bandwidth: bytes of K and V (2*B*Hkv*Nk*d*2) plus Q, O and LSE,
+    over the median time, against the measured HBM copy bandwidth."""
+    from attn_inputs import make_inputs
+    peaks, _ = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    B, Hq, Hkv, Nk, d = 8, 32, 8, 8192, 128
+    x = make_inputs(6, B, Hq, Hkv, Nk, d)
+    k, v = x["k"].to(dev), x["v"].to(dev)
+    res = {}
+    for nq in (1, 16, 128):
+        q = x["q"][:, :, Nk - nq:].contiguous().to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, nq), dtype=torch.float32, device=dev)
+        ws = torch.empty((max(A.attn_fwd_kv_workspace_size(B, Hq, Hkv, nq, Nk, d), 16),), dtype=torch.uint8,
+                         device=dev)
+        ms = _median_ms(torch, flush, lambda: A.attn_fwd_kv(q, k, v, causal=True, scale=d ** -0.5, o=o, lse=lse,
+                                                            workspace=ws))
+        nbytes = 2.0 * B * Hkv * Nk * d * 2 + 2.0 * B * Hq * nq * d * 2 + 4.0 * B * Hq * nq
+        gbs = nbytes / ms / 1e6
+        res[f"Nq{nq}"] = {"ms": round(ms, 4), "cache_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                          "grouped": A.attn_fwd_kv_workspace_size(B, Hq, Hkv, nq, Nk, d) > 0}
+    res["workload"] = "B8_Hq32_Hkv8_Nk8192_d128_causal"
+    res["hbm_peak_gbs"] = hbm
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout in the decode lines")
+    return res
+
+
+def rescale_lines(A, torch, dev):
+    """Conditional rescale on the grouped-head outlier workload (B=2, Hq=32, Hkv 8 and 1,
+    N=8192, d=128, causal): the number of (row, key block) steps after a row's first block
+    in which O was rescaled, with tau = 0 (every growth of the maximum) and tau = 8 (the
+    default), counted once each outside any timed region."""
+    from attn_inputs import make_inputs
+    res = {}
+    for hkv in (8, 1):
+        x = make_inputs(4, 2, 32, hkv, 8192, 128, recipe="outliers")
+        q, k, v = (x[nm].to(dev) for nm in ("q", "k", "v"))
+        counts = {}
+        for tau in (0.0, 8.0):
+            A.attn_set_debug_knobs(tau=tau)
+            A.attn_rescale_counter(True)
+            A.attn_fwd(q, k, v, causal=True, scale=128 ** -0.5)
+            counts[tau] = A.attn_rescale_counter(False)
+        A.attn_set_debug_knobs()
+        res[f"Hq32_Hkv{hkv}_N8192_causal"] = {
+            "rescales_tau0": counts[0.0], "rescales_tau8": counts[8.0],
+            "skipped_pct": round(100.0 * (1.0 - counts[8.0] / max(counts[0.0], 1)), 2)}
+        del x, q, k, v
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout in the rescale lines")
+    return res
+
+
+def _case_table():
+    """Single-configuration runs for a profiler (``--case NAME``): name -> (description,
+    setup(A, torch, dev) -> callable)."""
+    def fwd(b, h, hkv, n, d, causal, poly=0, recipe="normal", seed=3):
+        def setup(A, torch, dev):
+            from attn_inputs import make_inputs
+            x = make_inputs(seed, b, h, hkv, n, d, recipe=recipe)
+            q, k, v = (x[nm].to(dev) for nm in ("q", "k", "v"))
+            o, lse = torch.empty_like(q), torch.empty((b, h, n), dtype=torch.float32, device=dev)
+            A.attn_set_debug_knobs(poly_per_16=poly)
+            return lambda: A.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, o=o, lse=lse)
+        return setup
+
+    def bwd(b, h, n, d, causal, det=False, seed=5):
+        def setup(A, torch, dev):
+            from attn_inputs import make_inputs
+            x = make_inputs(seed, b, h, h, n, d, with_grad=True)
+            q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
+            o, lse = A.attn_fwd(q, k, v, causal=causal)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty((A.attn_bwd_workspace_size(b, h, h, n, d, det),), dtype=torch.uint8, device=dev)
+            return lambda: A.attn_bwd(q, k, v, o, lse, do, causal=causal, deterministic=det, dq=dq, dk=dk, dv=dv,
+                                      workspace=ws)
+        return setup
+
+    def varlen(backward, causal):
+        def setup(A, torch, dev):
+            from attn_inputs import make_varlen_inputs, varlen_workload
+            w = varlen_workload()
+            x = make_varlen_inputs(w["seed"], w["lens"], w["lens"], w["Hq"], w["Hkv"], w["d"])
+            q, k, v, cq, ck = (x[nm].to(dev) for nm in ("q", "k", "v", "cu_q", "cu_k"))
+            o, lse = A.attn_fwd_varlen(q, k, v, cq, ck, causal=causal)
+            if not backward:
+                return lambda: A.attn_fwd_varlen(q, k, v, cq, ck, causal=causal, o=o, lse=lse)
+            do = torch.randn(q.shape, generator=torch.Generator(device=dev).manual_seed(8),
+                             device=dev).to(torch.bfloat16)
+            return lambda: A.attn_bwd_varlen(q, k, v, o, lse, do, cq, ck, causal=causal)
+        return setup
+
+    def decode(nq):
+        def setup(A, torch, dev):
+            from attn_inputs import make_inputs
+            B, Hq, Hkv, Nk, d = 8, 32, 8, 8192, 128
+            x = make_inputs(6, B, Hq, Hkv, Nk, d)
+            k, v = x["k"].to(dev), x["v"].to(dev)
+            q = x["q"][:, :, Nk - nq:].contiguous().to(dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((B, Hq, nq), dtype=torch.float32, device=dev)
+            ws = torch.empty((max(A.attn_fwd_kv_workspace_size(B, Hq, Hkv, nq, Nk, d), 16),), dtype=torch.uint8,
+                             device=dev)
+            return lambda: A.attn_fwd_kv(q, k, v, causal=True, o=o, lse=lse, workspace=ws)
+        return setup
+
+    return {
+        "fwd_d128_N8192_noncausal": ("forward B2 H16 N8192 d128 non-causal", fwd(2, 16, 16, 8192, 128, False)),
+        "fwd_d128_N8192_noncausal_poly4": ("same, 4 of 16 exponentials on the FMA cubic",
+                                           fwd(2, 16, 16, 8192, 128, False, poly=4)),
+        "fwd_d128_N4096_noncausal": ("forward B4 H16 N4096 d128 non-causal", fwd(4, 16, 16, 4096, 128, False)),
+        "fwd_d64_N8192_noncausal": ("forward B2 H16 N8192 d64 non-causal", fwd(2, 16, 16, 8192, 64, False)),
+        "fwd_d256_N8192_noncausal": ("forward B2 H16 N8192 d256 non-causal (one-tile kernel)",
+                                     fwd(2, 16, 16, 8192, 256, False, seed=9)),
+        "fwd_gqa8_N8192_causal_outliers": ("forward B2 Hq32 Hkv8 N8192 d128 causal, outlier inputs",
+                                           fwd(2, 32, 8, 8192, 128, True, recipe="outliers", seed=4)),
+        "bwd_train_B4_H16_N2048": ("backward B4 H16 N2048 d128 non-causal", bwd(4, 16, 2048, 128, False, seed=2)),
+        "bwd_N8192_noncausal": ("backward B2 H16 N8192 d128 non-causal", bwd(2, 16, 8192, 128, False)),
+        "bwd_N8192_noncausal_det": ("same, deterministic dQ", bwd(2, 16, 8192, 128, False, det=True)),
+        "varlen_fwd_noncausal": ("packed forward, 18 sequences (65536 tokens), H16 d128", varlen(False, False)),
+        "varlen_bwd_noncausal": ("packed backward, same batch", varlen(True, False)),
+        "decode_Nq1": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 1 query", decode(1)),
+        "decode_Nq16": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 16 queries", decode(16)),
+    }
+
+
+def run_case(args):
+    """One configuration, --warmup untimed and --steps timed calls (CUDA events on the
+    current stream, no L2 flush): a short, single-kernel program for ncu."""
+    import torch
+    import attention_attn_fwd_09_gb300 as A
+    table = _case_table()
+    if args.case not in table:
+        raise SystemExit(f"unknown case {args.case!r}; cases: {', '.join(sorted(table))}")
+    desc, setup = table[args.case]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    call = setup(A, torch, dev)
+    for _ in range(args.warmup):
+        call()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for e in evs:
+        e[0].record()
+        call()
+        e[1].record()
+    torch.cuda.synchronize()
+    A.attn_set_debug_knobs()
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout")
+    return {"case": args.case, "what": desc, "steps": args.steps, "warmup": args.warmup,
+            "median_ms": round(statistics.median(e[0].elapsed_time(e[1]) for e in evs), 4)}
+
+
 def run_ours(args):
     import torch
 
@@ -553,6 +713,8 @@ def run_ours(args):
         varlen = varlen_lines(A, torch, dev, flush)
         wide = wide_lines(A, torch, dev, flush)
         suite = suite_lines(A, torch, dev, flush)
+        decode = decode_lines(A, torch, dev, flush)
+        rescale = rescale_lines(A, torch, dev)
 
     peaks, peak_src = measured_peaks()
     fwd_avg = statistics.mean(fwd_ms)
@@ -593,6 +755,8 @@ def run_ours(args):
         out["varlen_mixed_lengths"] = varlen
         out["fwd_wide_heads"] = wide
         out["suite"] = suite
+        out["decode_kv_cache"] = decode
+        out["rescale_skip_outliers"] = rescale
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()
         out["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": host_cores(),
@@ -648,7 +812,10 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.case is not None:
+        out = run_case(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -18,8 +18,9 @@
  *    K, V, dK, dV are [B, Hkv, N, d].  LSE is fp32 [B, Hq, N].
  *  - Grouped heads (GQA/MQA): Hq must be a multiple of Hkv; query head h reads
  *    key/value head h / (Hq / Hkv).
- *  - d must be 64 or 128.  N >= 0, B >= 0 (either being 0 is a no-op returning 0).
- *    Any N >= 1 is supported (a ragged last tile is masked).
+ *  - Head dim d: each entry point states the values it takes (64 and 128 everywhere;
+ *    the forward entry points also 192 and 256).  N >= 0, B >= 0 (either being 0 is a
+ *    no-op returning 0).  Any N >= 1 is supported (a ragged last tile is masked).
  *  - Every tensor pointer must be 16-byte aligned (TMA requirement).
  *  - scale > 0 (the usual choice is 1/sqrt(d)).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous:
@@ -220,7 +221,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * the process exits).  Sizes whose attn_bwd_workspace_size exceeds 64 MiB are rejected
  * with ATTN_ERR_WORKSPACE and a message in attn_last_error().  Nothing is allocated.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.  All calls
+ * with that device current (a failed lookup returns ATTN_ERR_CUDA and is tried again on
+ * the next call); make that first call before any stream capture.  All calls
  * share the array and it keeps the last call's contents (the backward clears what must
  * start at zero itself), so calls that overlap on the GPU, e.g. on two streams, race.
  */

@@ -83,12 +83,14 @@ def test_long_atomic_and_deterministic(A, N, causal):
         torch.cuda.synchronize()
         assert A.attn_device_status(True) == 0
         outs[det] = tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
-    sel = [(w["B"] - 1, w["Hkv"] - 1)]
+    # The first and the last K/V head: the grid's first CTAs and its tail.
+    sel = [(0, 0), (w["B"] - 1, w["Hkv"] - 1)]
     dQ, dK, dV = oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], causal, scale, kv_heads=sel)
-    b, h = sel[0]
-    for det in (False, True):
-        dq, dk, dv = outs[det]
-        check((dq[b, h:h + 1], dk[b, h], dv[b, h]), (dQ[0], dK[0], dV[0]), f"N{N} causal={causal} det={det}")
+    for s, (b, h) in enumerate(sel):
+        for det in (False, True):
+            dq, dk, dv = outs[det]
+            check((dq[b, h:h + 1], dk[b, h], dv[b, h]), (dQ[s], dK[s], dV[s]),
+                  f"N{N} causal={causal} det={det} b{b} h{h}")
     for i in range(3):   # atomic and ordered accumulation agree everywhere
         assert rel_fro(outs[True][i], outs[False][i]) <= GRAD_REL_FRO
 
