@@ -8,7 +8,8 @@ imports it, and this package imports nothing from the product path.
 ``attn_fwd_varlen``, packed sequences of different lengths, built on it) wrap
 the plain-C fp64 implementation in ``attn_oracle.c``
 (materialised S and P, chain-rule gradients); ``tiled`` holds a step-by-step fp32
-emulation of the tiled online softmax with the conditional rescale.
+emulation of the tiled online softmax with the conditional rescale; ``fp8`` holds the
+e4m3 encoding, the per-block quantiser and the fp64 forward of dequantised FP8 inputs.
 """
 from __future__ import annotations
 
