@@ -6,7 +6,8 @@ library is missing this module raises at import time; there is no fallback.
 
 Names match the C ABI in include/attn.h: ``attn_fwd``, ``attn_fwd_kv``,
 ``attn_fwd_varlen`` and ``attn_bwd_varlen`` (packed sequences of different lengths), ``attn_bwd``,
-``attn_bwd_noalloc``, the ``*_workspace_size`` queries, ``attn_last_error`` and the
+``attn_bwd_noalloc``, ``attn_quantize_fp8`` and ``attn_fwd_fp8`` (e4m3 inputs with
+per-block scales), the ``*_workspace_size`` queries, ``attn_last_error`` and the
 test/tuning knobs.
 """
 from __future__ import annotations
@@ -66,6 +67,10 @@ _lib.attn_rescale_counter.argtypes = [_i, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.attn_rescale_counter.restype = _i
 _lib.attn_set_test_hooks.argtypes = [_i]
 _lib.attn_set_test_hooks.restype = _i
+_lib.attn_quantize_fp8.argtypes = [_p, _p, _p, _i, _i, _i, _i, _p]
+_lib.attn_quantize_fp8.restype = _i
+_lib.attn_fwd_fp8.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]
+_lib.attn_fwd_fp8.restype = _i
 _lib.attn_exp2_sw.argtypes = [_p, _p, _ll, _i, _p]
 _lib.attn_exp2_sw.restype = _i
 
@@ -333,6 +338,46 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, causal: bool = False, scale: float | N
     return dq, dk, dv
 
 
+def attn_quantize_fp8(x, x8=None, scales=None, stream=None):
+    """e4m3 codes and per-128-row-block fp32 scales of x [B,H,N,128] bf16 (CUDA).  Returns
+    (x8 uint8 [B,H,N,128], scales fp32 [B,H,ceil(N/128)])."""
+    B, H, N, d = x.shape
+    _dev_bf16("x", x, (B, H, N, d))
+    nb = (N + 127) // 128
+    x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device) if x8 is None else x8
+    scales = torch.empty((B, H, nb), dtype=torch.float32, device=x.device) if scales is None else scales
+    if x8.dtype != torch.uint8 or not x8.is_contiguous() or tuple(x8.shape) != (B, H, N, d) or x8.device != x.device:
+        raise ValueError("x8: expected a contiguous uint8 tensor shaped like x on its device")
+    _dev_f32("scales", scales, (B, H, nb))
+    _check(_lib.attn_quantize_fp8(_ptr(x), _ptr(x8), _ptr(scales), B, H, N, d, _stream(stream)))
+    return x8, scales
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, scale: float | None = None, o=None,
+                 lse=None, stream=None):
+    """O, LSE of the FP8 inputs (e4m3 codes as uint8 tensors q8 [B,Hq,N,128], k8/v8
+    [B,Hkv,N,128], fp32 block scales [.., ceil(N/128)] as attn_quantize_fp8 returns them).
+    O is bf16, LSE fp32."""
+    B, Hq, N, d = q8.shape
+    Hkv = k8.shape[1]
+    nb = (N + 127) // 128
+    for name, t, shp in (("q8", q8, (B, Hq, N, d)), ("k8", k8, (B, Hkv, N, d)), ("v8", v8, (B, Hkv, N, d))):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"{name}: expected a contiguous CUDA uint8 tensor of shape {shp}")
+    _dev_f32("q_scale", q_scale, (B, Hq, nb))
+    _dev_f32("k_scale", k_scale, (B, Hkv, nb))
+    _dev_f32("v_scale", v_scale, (B, Hkv, nb))
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _dev_bf16("o", o, (B, Hq, N, d))
+    _dev_f32("lse", lse, (B, Hq, N))
+    _check(_lib.attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(o),
+                             _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream(stream)))
+    return o, lse
+
+
 def attn_set_debug_knobs(tau: float = 8.0, poly_per_16: int = 0, wait_limit_ns: int = 2_000_000_000,
                          sync_check: bool = False):
     _check(_lib.attn_set_debug_knobs(float(tau), int(poly_per_16), int(wait_limit_ns), int(bool(sync_check))))
@@ -369,6 +414,6 @@ def attn_exp2_sw(x, variant: int = 0, stream=None):
     return y
 
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_last_error", "attn_version",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_quantize_fp8", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_last_error", "attn_version",
            "attn_set_debug_knobs", "attn_get_debug_knobs", "attn_device_status", "attn_rescale_counter",
            "attn_exp2_sw", "attn_set_test_hooks", "AttnError", "LIB_PATH"]

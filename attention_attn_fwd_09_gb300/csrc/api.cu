@@ -119,6 +119,22 @@ int make_map(CUtensorMap* m, const void* base, int d, int rows, long long bh, co
   return ATTN_OK;
 }
 
+// [BH, rows, 128] e4m3 tensor (one byte per element), boxes of 128 rows x 128 bytes,
+// 128-byte swizzle: one box is a whole 128 x 128 tile.
+int make_map_e4m3(CUtensorMap* m, const void* base, int rows, long long bh, const char* name) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(g_encode_err));
+  cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {128, (cuuint64_t)rows * 128};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "tensor map for %s: CUresult %d", name, (int)r);
+  return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // wide: the forward also takes d = 192 and 256 (one-tile kernel, fwd_wide.cu).
@@ -472,6 +488,77 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   if (e != cudaSuccess) return cuda_fail(e, "unit table launch");
   e = wide ? launch_fwd_wide(maps, p, d, (int)cap, st) : launch_fwd(maps, p, d, 0, (int)cap, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return post_launch(s, st);
+}
+
+int attn_quantize_fp8(const void* x, void* x8, float* scales, int B, int H, int N, int d, void* stream) {
+  if (B < 0 || H <= 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "B=%d, H=%d, N=%d: need B, N >= 0 and H >= 1", B, H, N);
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (the FP8 path supports 128)", d);
+  if (B == 0 || N == 0) return ATTN_OK;
+  if ((long long)B * H * ((N + 127) / 128) > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "too many blocks");
+  if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return fail(ATTN_ERR_MISALIGNED, "x and x8 must be 16-byte aligned, scales 4-byte aligned");
+  cudaError_t e = launch_quantize_fp8(x, x8, scales, (long long)B * H, N, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                 float scale, void* stream) {
+  int rc = check_shape(B, Hq, Hkv, N, d == 128 ? 128 : 0, scale);
+  if (rc != ATTN_OK) {
+    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (the FP8 path supports 128)", d);
+    return rc;
+  }
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale || !o || !lse)
+    return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_MISALIGNED, "q8, k8, v8, o and lse must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_MISALIGNED, "the scale arrays must be 4-byte aligned");
+  int dev = 0;
+  const DevSyms* s = dev_syms(&dev);
+  if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
+  FwdMaps maps;
+  if ((rc = make_map_e4m3(&maps.q, q8, N, (long long)B * Hq, "q8")) != ATTN_OK) return rc;
+  if ((rc = make_map_e4m3(&maps.k, k8, N, (long long)B * Hkv, "k8")) != ATTN_OK) return rc;
+  if ((rc = make_map_e4m3(&maps.v, v8, N, (long long)B * Hkv, "v8")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.o, o, 128, N, (long long)B * Hq, "o")) != ATTN_OK) return rc;
+  FwdParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv;
+  p.Nk = N; p.koff = 0;
+  p.causal = causal ? 1 : 0;
+  p.pair_heads = (p.g >= 2 && p.g % 2 == 0) ? 1 : 0;
+  p.n_qblk = (N + 127) / 128;
+  p.n_kvblk = p.n_qblk;
+  p.n_rowslots = p.pair_heads ? p.n_qblk : (p.n_qblk + 1) / 2;
+  p.units_per_row = p.pair_heads ? B * (Hq / 2) : B * Hq;
+  p.c = scale * 1.4426950408889634f;
+  p.tau = g_tau.load();
+  p.lse = lse;
+  p.wait_ns = (unsigned long long)g_wait_ns.load();
+  p.status = s->status;
+  p.rescale_count = g_count_rescales.load() ? s->rescale : nullptr;
+  p.test_skip_first_kv = g_test_skip_kv.load();
+  // Two-tile units, the last partial wave split into one-tile CTAs (as attn_fwd).
+  const long long units = (long long)p.n_rowslots * p.units_per_row;
+  p.split_from = (int)std::min<long long>(units, 0x7fffffffLL);
+  if (!p.causal) {
+    const long long sms = std::max(1, s->sms);
+    const long long rem = units % sms;
+    if (units >= sms && rem > 0 && 2 * rem <= sms) p.split_from = (int)(units - rem);
+    else if (units < sms && 2 * units <= sms) p.split_from = 0;
+  }
+  const long long grid = p.split_from + 2 * (units - p.split_from);
+  if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+  const Fp8Scales sc{q_scale, k_scale, v_scale};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_fwd_fp8(maps, p, sc, (int)grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 forward launch");
   return post_launch(s, st);
 }
 

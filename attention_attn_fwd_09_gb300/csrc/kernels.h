@@ -86,6 +86,18 @@ cudaError_t launch_fwd_persistent(const FwdMaps& maps, const FwdParams& p, int D
 // grid = B * Hq * ceil(N / 128); same parameters as launch_fwd (ordinary mode only).
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t stream);
 
+// FP8 forward (fwd_fp8.cu), d = 128, ordinary tiling: Q/K/V maps over e4m3 bytes (boxes
+// of 128 rows x 128 bytes), O map as for launch_fwd; block scales per 128 rows of a head.
+struct Fp8Scales {
+  const float* q;   // [B, Hq, ceil(N / 128)]
+  const float* k;   // [B, Hkv, ceil(N / 128)]
+  const float* v;   // [B, Hkv, ceil(N / 128)]
+};
+cudaError_t launch_fwd_fp8(const FwdMaps& maps, const FwdParams& p, const Fp8Scales& sc, int grid, cudaStream_t stream);
+size_t fwd_fp8_smem_bytes();
+// Block quantiser: x bf16 [heads, N, 128] -> x8 e4m3 [heads, N, 128], scales [heads, ceil(N / 128)].
+cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, long long heads, int N, cudaStream_t stream);
+
 // Software exp2 accuracy / throughput test entry: variant 0 = production polynomial,
 // 1 = full-range polynomial, 2 = MUFU ex2.approx.
 cudaError_t launch_exp2_test(const float* x, float* y, long long n, int variant, cudaStream_t s);

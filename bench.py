@@ -385,6 +385,41 @@ def suite_lines(A, torch, dev, flush):
     return res
 
 
+def fp8_lines(A, torch, dev, flush):
+    """FP8 forward (e4m3 Q/K/V with per-128-row block scales, d = 128) at the forward
+    sweep's shapes (B = 16384 / N, 16 heads): TFLOP/s with the same FLOP count as the bf16
+    forward, next to the bf16 forward on the same inputs, and the quantiser's bandwidth
+    (2 bytes read and 1 written per element, plus the scales)."""
+    peaks, _ = measured_peaks()
+    res = {}
+    for n in (4096, 8192, 16384):
+        b = 16384 // n
+        g = torch.Generator(device=dev).manual_seed(3)
+        q, k, v = (torch.randn((b, 16, n, 128), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+        q8, sq = A.attn_quantize_fp8(q)
+        k8, sk = A.attn_quantize_fp8(k)
+        v8, sv = A.attn_quantize_fp8(v)
+        o, lse = torch.empty_like(q), torch.empty((b, 16, n), dtype=torch.float32, device=dev)
+        for causal in (False, True):
+            ms = _median_ms(torch, flush, lambda: A.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal,
+                                                                 scale=128 ** -0.5, o=o, lse=lse))
+            ms16 = _median_ms(torch, flush, lambda: A.attn_fwd(q, k, v, causal=causal, scale=128 ** -0.5, o=o,
+                                                               lse=lse))
+            fl = fwd_flops(b, 16, n, 128, causal)
+            res[f"N{n}_{'causal' if causal else 'noncausal'}"] = {
+                "B": b, "ms": round(ms, 4), "tflops": round(fl / ms / 1e9, 1), "bf16_ms": round(ms16, 4),
+                "bf16_tflops": round(fl / ms16 / 1e9, 1)}
+        if n == 4096:
+            msq = _median_ms(torch, flush, lambda: A.attn_quantize_fp8(q, q8, sq))
+            nbytes = 3.0 * q.numel() + 4.0 * sq.numel()
+            res["quantize_B4_H16_N4096"] = {"ms": round(msq, 4), "gbs": round(nbytes / msq / 1e6, 1),
+                                            "frac_of_hbm": round(nbytes / msq / 1e6 / float(peaks["hbm_gbs"]), 4)}
+        del q, k, v, q8, k8, v8, o, lse
+    if A.attn_device_status(True) != 0:
+        raise RuntimeError("a kernel reported a timeout in the FP8 lines")
+    return res
+
+
 def decode_lines(A, torch, dev, flush):
     """Decoding against a key/value cache (attn_fwd_kv): B=8, Hq=32, Hkv=8, Nk=8192, d=128,
     causal, Nq new queries per head.  The forward reads the whole cache once, so the line
@@ -481,6 +516,15 @@ def _case_table():
             return lambda: A.attn_bwd_varlen(q, k, v, o, lse, do, cq, ck, causal=causal)
         return setup
 
+    def fwd_fp8(b, n, causal):
+        def setup(A, torch, dev):
+            g = torch.Generator(device=dev).manual_seed(3)
+            q, k, v = (torch.randn((b, 16, n, 128), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+            (q8, sq), (k8, sk), (v8, sv) = (A.attn_quantize_fp8(t) for t in (q, k, v))
+            o, lse = torch.empty_like(q), torch.empty((b, 16, n), dtype=torch.float32, device=dev)
+            return lambda: A.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal, o=o, lse=lse)
+        return setup
+
     def decode(nq):
         def setup(A, torch, dev):
             from attn_inputs import make_inputs
@@ -510,6 +554,8 @@ def _case_table():
         "bwd_N8192_noncausal_det": ("same, deterministic dQ", bwd(2, 16, 8192, 128, False, det=True)),
         "varlen_fwd_noncausal": ("packed forward, 18 sequences (65536 tokens), H16 d128", varlen(False, False)),
         "varlen_bwd_noncausal": ("packed backward, same batch", varlen(True, False)),
+        "fp8_fwd_N8192_noncausal": ("FP8 forward B2 H16 N8192 d128 non-causal", fwd_fp8(2, 8192, False)),
+        "fp8_fwd_N4096_noncausal": ("FP8 forward B4 H16 N4096 d128 non-causal", fwd_fp8(4, 4096, False)),
         "decode_Nq1": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 1 query", decode(1)),
         "decode_Nq16": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 16 queries", decode(16)),
     }
@@ -714,6 +760,7 @@ def run_ours(args):
         wide = wide_lines(A, torch, dev, flush)
         suite = suite_lines(A, torch, dev, flush)
         decode = decode_lines(A, torch, dev, flush)
+        fp8 = fp8_lines(A, torch, dev, flush)
         rescale = rescale_lines(A, torch, dev)
 
     peaks, peak_src = measured_peaks()
@@ -756,6 +803,7 @@ def run_ours(args):
         out["fwd_wide_heads"] = wide
         out["suite"] = suite
         out["decode_kv_cache"] = decode
+        out["fwd_fp8_e4m3"] = fp8
         out["rescale_skip_outliers"] = rescale
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, secs, desc = oracle_sample()

@@ -90,6 +90,38 @@ int attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse
                 int Nk, int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 inputs ("Hotelren FA4 summary" page, section 6.3, future directions: FP8 inputs; the
+ * reverse-engineering page's FP8 path).  The pages fix neither the format nor the scaling;
+ * this library reads them as e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * largest value 448, no infinities) with one fp32 scale per block of 128 consecutive rows
+ * of one head: the value of an element is decode(code) * scale of its block.
+ *
+ * attn_quantize_fp8: x [B,H,N,d] bf16 in -> x8 [B,H,N,d] e4m3 codes (one byte each) and
+ *   scales [B,H,ceil(N/128)] fp32 out.  Per block: amax = max |x|, scale = amax / 448 in
+ *   fp32 (1 for an all-zero block), code = e4m3(x / scale) rounded to nearest even,
+ *   saturating at +-448.  d must be 128.  x and x8 16-byte aligned, scales 4-byte aligned;
+ *   all three caller-owned device memory.
+ */
+int attn_quantize_fp8(const void* x, void* x8, float* scales, int B, int H, int N, int d, void* stream);
+
+/*
+ * FP8 forward: O = softmax(scale * Q~ K~^T [causal]) V~ and LSE, where Q~, K~, V~ are the
+ * dequantised inputs.  The score product runs on the 8-bit tensor path; P is kept at 16 bits
+ * (fp16, times V's block scale) and V is widened exactly to fp16 on chip for O += P V, so the
+ * result meets the bf16 forward's error bounds against the exact attention of Q~, K~, V~.
+ *
+ *   q8 [B,Hq,N,128], k8, v8 [B,Hkv,N,128] e4m3 codes (16-byte aligned);
+ *   q_scale [B,Hq,ceil(N/128)], k_scale, v_scale [B,Hkv,ceil(N/128)] fp32, positive
+ *       and finite (as attn_quantize_fp8 writes them; 256 * v_scale must stay below
+ *       65504, i.e. |V| below about 1.1e5, so that P * v_scale fits fp16 with tau = 8);
+ *   o [B,Hq,N,128] bf16, lse [B,Hq,N] fp32 out; d must be 128; other arguments, ownership
+ *   and errors as attn_fwd.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                 float scale, void* stream);
+
+/*
  * Bytes of workspace attn_fwd_kv uses for these sizes on the current device (0 when it
  * packs nothing); (size_t)-1 for invalid sizes.
  */

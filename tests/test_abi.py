@@ -168,3 +168,27 @@ def test_bwd_varlen_workspace_and_errors(lib):
     assert call(ws=MIS) == -3
     assert call(cu=ctypes.c_void_p(0x10001)) == -3
     assert call(tq=0, tk=0) == 0
+
+
+def test_fp8_argument_errors(lib):
+    # Host-side checks of the FP8 entry points, before any device work.
+    lib.attn_quantize_fp8.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    lib.attn_quantize_fp8.restype = ctypes.c_int
+    p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd_fp8.argtypes = [p] * 8 + [i] * 6 + [f, p]
+    lib.attn_fwd_fp8.restype = i
+    assert lib.attn_quantize_fp8(FAKE, FAKE, FAKE, 1, 2, 128, 64, None) == -2
+    assert b"128" in lib.attn_last_error()
+    assert lib.attn_quantize_fp8(FAKE, FAKE, None, 1, 2, 128, 128, None) == -1
+    assert lib.attn_quantize_fp8(FAKE, MIS, FAKE, 1, 2, 128, 128, None) == -3
+    assert lib.attn_quantize_fp8(FAKE, FAKE, FAKE, 1, 2, 0, 128, None) == 0
+
+    def call(d=128, Hq=2, Hkv=2, N=128, scale=0.1, q8=FAKE, ks=FAKE):
+        return lib.attn_fwd_fp8(q8, FAKE, FAKE, FAKE, ks, FAKE, FAKE, FAKE, 1, Hq, Hkv, N, d, 0, scale, None)
+    assert call(d=64) == -2 and b"FP8" in lib.attn_last_error()
+    assert call(Hq=3) == -1
+    assert call(scale=-1.0) == -1
+    assert call(q8=None) == -1
+    assert call(q8=MIS) == -3
+    assert call(ks=ctypes.c_void_p(0x10002)) == -3
+    assert call(N=0) == 0
