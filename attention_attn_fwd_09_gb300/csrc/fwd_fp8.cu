@@ -15,8 +15,9 @@
 //     sq * sk_j, and log2(sv_j) is added to it, so the exponential unit returns p * sv_j
 //     directly; the row sum l accumulates p itself (the block sum divided by sv_j);
 //   * P * sv_j is stored to tensor memory as fp16 (11-bit significand, finer than bf16), and
-//     V8 is widened to fp16 in shared memory by two converter warps (e4m3 -> fp16 is exact),
-//     so O += P V~ runs on the 16-bit path (kind::f16 with f16 operands).  Keeping P at 16
+//     V8 is widened to fp16 in shared memory by the correction warpgroup, which is idle
+//     between its rare rescales (e4m3 -> fp16 is exact), so O += P V~ runs on the 16-bit
+//     path (kind::f16 with f16 operands).  Keeping P at 16
 //     bits keeps the forward's error within the bf16 path's bounds against the exact
 //     attention of the dequantised inputs; an e4m3 P (3 mantissa bits) would not be;
 //   * O accumulates sum_j (p sv_j) V8_j = sum_j p V~_j in fp32, and the epilogue divides by l.
@@ -71,8 +72,8 @@ enum {
   E_DONE = 11,
   E_KFULL = 12,    // +slot (2)
   E_V8FULL = 14,   // +slot (3)
-  E_V8EMPTY = 17,  // +slot (3): the converters have read the slot (64 arrivals)
-  E_V16FULL = 20,  // +slot (2): the converters have written the slot (64 arrivals)
+  E_V8EMPTY = 17,  // +slot (3): the correction warpgroup has read the slot (128 arrivals)
+  E_V16FULL = 20,  // +slot (2): the correction warpgroup has written the slot (128 arrivals)
   E_EPI = 22,      // +t
   E_FIN = 24,      // +t
   E_COUNT = 26
@@ -134,6 +135,45 @@ __device__ __forceinline__ F8Tiles f8_unit(const FwdParams& p, int unit) {
   return T;
 }
 
+// V8 block j (128 keys x 128 e4m3, 128-byte swizzled rows as TMA lands them) -> fp16 in the
+// layout the PV product reads (two 64-column boxes with 128-byte swizzle, the layout TMA
+// gives a bf16 V tile).  128 threads; a 16-byte piece (r, u) is columns 16u .. 16u + 15 of
+// key row r.  Each quarter-warp takes half of two adjacent rows, (r, u in 0..3) with
+// (r + 1, u in 4..7) or the other way round, so that its eight 16-byte loads and each of
+// its two rounds of 16-byte stores fall on eight distinct bank groups.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t pair) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));   // low byte -> low half
+  return r;
+}
+__device__ __forceinline__ void widen_v_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int ct) {
+  const int w = ct >> 5, l = ct & 31;
+  const int quarter = l >> 3, lq = l & 7;
+  const int half = lq >> 2;                                  // which row of the pair
+  const int u = (lq & 3) + 4 * (half ^ (quarter & 1));
+  // Rows r = 16 it + r0 (it = 0..7); r & 7 = r0 & 7 for every it, so each address is a
+  // per-thread base plus an immediate.
+  const int r0 = 4 * w + 2 * (quarter >> 1) + half, sw = r0 & 7;
+  const uint8_t* s_base = src + r0 * 128 + ((u ^ sw) << 4);
+  uint8_t* d_base = dst + (u >> 2) * F8Cfg::CH16 + r0 * 128;
+  const int d0 = ((2 * (u & 3)) ^ sw) << 4, d1 = ((2 * (u & 3) + 1) ^ sw) << 4;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s_base + it * 2048);
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint16_t lo, hi;
+      asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(in[i]));
+      h[2 * i] = e4m3x2_to_f16x2(lo);
+      h[2 * i + 1] = e4m3x2_to_f16x2(hi);
+    }
+    *reinterpret_cast<uint4*>(d_base + it * 2048 + d0) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(d_base + it * 2048 + d1) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 __global__ void __launch_bounds__(kF8Threads, 1)
     attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -180,12 +220,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_init(BAR(E_EPI + t), 128);
       mbar_init(BAR(E_FIN + t), 128);
       mbar_init(BAR(E_KFULL + t), 1);
-      mbar_init(BAR(E_V16FULL + t), 64);
+      mbar_init(BAR(E_V16FULL + t), 128);
     }
     mbar_init(BAR(E_DONE), 1);
     for (int s = 0; s < C::NV8; ++s) {
       mbar_init(BAR(E_V8FULL + s), 1);
-      mbar_init(BAR(E_V8EMPTY + s), 64);
+      mbar_init(BAR(E_V8EMPTY + s), 128);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -199,8 +239,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Register split against the launch's 128 x 512: producer, MMA and the two converter
-  // warps 64; softmax 184 each; correction 80.
+  // Register split against the launch's 128 x 512: producer and MMA 64; softmax 184 each;
+  // correction (and V widening) 80.
   if (wg == 0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
     if (warp == 0) {
@@ -295,42 +335,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         while (!mbar_try_wait(BAR(E_DONE), 0) && globaltimer_ns() - t0 < p.wait_ns) {
         }
       }
-    } else {
-      // ---------------------------------------------------------------- converters (warps 2, 3)
-      // V8 block j (128 keys x 128 e4m3, 128-byte swizzled rows) -> fp16 in the layout the
-      // PV product reads (two 64-column boxes, 128-byte swizzle: the layout TMA gives a
-      // bf16 V tile).  Thread ct takes 16-byte pieces ct, ct + 64, ...: piece (r, u) holds
-      // columns 16u .. 16u + 15 of key row r.
-      const int ct = (int)threadIdx.x - 64;
-      for (int j = 0; j < nmax; ++j) {
-        const int vs8 = j % C::NV8, vs16 = j % C::NV16;
-        if (!f8_warp_wait(BAR(E_V8FULL + vs8), (j / C::NV8) & 1, wc)) break;
-        // V16 slot vs16 last held block j - 2, released with group j - 1.
-        if (j >= C::NV16 && !f8_warp_wait(BAR(E_REL + ((j - 1) & 1)), ((j - 1) >> 1) & 1, wc)) break;
-        const uint8_t* src = smem + C::OFF_V8 + vs8 * C::T8;
-        uint8_t* dst = smem + C::OFF_V16 + vs16 * C::T16;
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-          const int piece = it * 64 + ct, r = piece >> 3, u = piece & 7;
-          const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((u ^ (r & 7)) << 4));
-          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] & 0xffffu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] >> 16), __NV_E4M3);
-            h[2 * i] = uint32_t(lo.x) | (uint32_t(lo.y) << 16);
-            h[2 * i + 1] = uint32_t(hi.x) | (uint32_t(hi.y) << 16);
-          }
-          uint8_t* box = dst + (u >> 2) * C::CH16 + r * 128;
-          const int s0 = (u & 3) * 2;
-          *reinterpret_cast<uint4*>(box + ((s0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(box + (((s0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        fence_proxy_async_smem();   // generic writes -> tensor-core reads
-        mbar_arrive(BAR(E_V16FULL + vs16));
-        mbar_arrive(BAR(E_V8EMPTY + vs8));
-      }
     }
   } else if (wg == 1 || wg == 2) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
@@ -418,7 +422,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     // ------------------------------------------------------------------ correction + epilogue
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    bool ok = true;
+    const int ct = (int)threadIdx.x - 384;
+    // Widen V8 block jj into V16 slot jj % 2 once it has landed and the slot's previous
+    // block (jj - 2) has been read by its PV products (released with group jj - 1).
+    auto widen = [&](int jj) -> bool {
+      const int vs8 = jj % C::NV8, vs16 = jj % C::NV16;
+      if (!f8_warp_wait(BAR(E_V8FULL + vs8), (jj / C::NV8) & 1, wc)) return false;
+      if (jj >= C::NV16 && !f8_warp_wait(BAR(E_REL + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, wc)) return false;
+      widen_v_tile(smem + C::OFF_V8 + vs8 * C::T8, smem + C::OFF_V16 + vs16 * C::T16, ct);
+      fence_proxy_async_smem();   // generic writes -> tensor-core reads
+      mbar_arrive(BAR(E_V16FULL + vs16));
+      mbar_arrive(BAR(E_V8EMPTY + vs8));
+      return true;
+    };
+    bool ok = nmax == 0 || widen(0);
     for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -450,6 +467,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tc_fence_before();
         mbar_arrive(BAR(E_PFULL + t));
       }
+      // The next block's V, needed by the PV products two MMA iterations from now.
+      if (ok && j + 1 < nmax && !widen(j + 1)) ok = false;
     }
     // Epilogue: once every product of both tiles has completed (the V16 slots, which stage
     // O, are then free), per tile O / l -> bf16 -> V16 slot t -> TMA store, and the LSE.
