@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 ROOT = os.path.dirname(PKG)
-SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "fwd_persist.cu", "fwd_fp8.cu", "bwd.cu", "noalloc.cu", "varlen.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "fwd_persist.cu", "fwd_fp8.cu", "bwd.cu", "bwd_wide.cu", "noalloc.cu", "varlen.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-diag-suppress", "177"]

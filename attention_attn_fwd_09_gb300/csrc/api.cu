@@ -576,18 +576,21 @@ int attn_exp2_sw(const float* x, float* y, long long n, int variant, void* strea
 extern "C" {
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int deterministic) {
-  if (check_shape(B, Hq, Hkv, N, d, 1.0f) != ATTN_OK) return (size_t)-1;
+  if (check_shape(B, Hq, Hkv, N, d, 1.0f, true) != ATTN_OK) return (size_t)-1;
   if (B == 0 || N == 0) return 0;
+  if (d > 128) return bwd_wide_workspace_bytes(B, Hq, N, d, deterministic);
   return bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
              void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_shape(B, Hq, Hkv, N, d, scale);
+  int rc = check_shape(B, Hq, Hkv, N, d, scale, true);
   if (rc != ATTN_OK) return rc;
   if (B == 0 || N == 0) return ATTN_OK;
-  const size_t need = bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
+  const bool wide = d > 128;   // d = 192, 256: bwd_wide.cu
+  const size_t need = wide ? bwd_wide_workspace_bytes(B, Hq, N, d, deterministic)
+                           : bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
   if (!workspace || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
@@ -598,10 +601,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   const DevSyms* s = dev_syms(&dev);
   if (s->err != cudaSuccess) return cuda_fail(s->err, "device setup");
   BwdMaps maps;
-  if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q")) != ATTN_OK) return rc;
+  const int qrows = wide ? 64 : 128;   // query tile rows of the kernel
+  if ((rc = make_map(&maps.q, q, d, N, (long long)B * Hq, "q", qrows)) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.k, k, d, N, (long long)B * Hkv, "k")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.v, v, d, N, (long long)B * Hkv, "v")) != ATTN_OK) return rc;
-  if ((rc = make_map(&maps.dout, dout, d, N, (long long)B * Hq, "dout")) != ATTN_OK) return rc;
+  if ((rc = make_map(&maps.dout, dout, d, N, (long long)B * Hq, "dout", qrows)) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.dk, dk, d, N, (long long)B * Hkv, "dk")) != ATTN_OK) return rc;
   if ((rc = make_map(&maps.dv, dv, d, N, (long long)B * Hkv, "dv")) != ATTN_OK) return rc;
   BwdParams p{};
@@ -612,11 +616,12 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.c = scale * 1.4426950408889634f;
   p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  bwd_workspace_carve(workspace, B, Hq, Hkv, N, d, deterministic, &p);
+  if (wide) bwd_wide_workspace_carve(workspace, B, Hq, N, d, deterministic, &p);
+  else bwd_workspace_carve(workspace, B, Hq, Hkv, N, d, deterministic, &p);
   p.wait_ns = (unsigned long long)g_wait_ns.load();
   p.status = s->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bwd(maps, p, st);
+  cudaError_t e = wide ? launch_bwd_wide(maps, p, st) : launch_bwd(maps, p, st);
   if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward not available for these arguments");
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return post_launch(s, st);

@@ -139,5 +139,11 @@ struct BwdVarlenLayout {
 BwdVarlenLayout bwd_varlen_layout(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
 // Points p->dq_acc, delta, lse2, sem into the caller's workspace.
 void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int deterministic, BwdParams* p);
+// Backward for d = 192, 256 (bwd_wide.cu): maps as launch_bwd except q and dout, whose
+// boxes are 64 rows; workspace: dQacc [B, Hq, ceil(N/64)*64, d], D and LSE2 [B, Hq, N],
+// counters [B, Hq, ceil(N/64), 2] when deterministic.
+size_t bwd_wide_workspace_bytes(int B, int Hq, int N, int d, int deterministic);
+void bwd_wide_workspace_carve(void* ws, int B, int Hq, int N, int d, int deterministic, BwdParams* p);
+cudaError_t launch_bwd_wide(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace attn
