@@ -45,6 +45,8 @@ _lib.attn_set_fwd_persistent.argtypes = [_i]
 _lib.attn_set_fwd_persistent.restype = _i
 _lib.attn_set_fwd_one_tile.argtypes = [_i]
 _lib.attn_set_fwd_one_tile.restype = _i
+_lib.attn_set_bwd_query_tile.argtypes = [_i]
+_lib.attn_set_bwd_query_tile.restype = _i
 _lib.attn_set_varlen_order.argtypes = [_i]
 _lib.attn_set_varlen_order.restype = _i
 _lib.attn_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]
@@ -296,6 +298,12 @@ def attn_set_fwd_persistent(enable: bool):
 def attn_set_fwd_one_tile(enable: bool):
     """d = 128 forward kernel: one query tile per CTA (True) or two (False)."""
     _check(_lib.attn_set_fwd_one_tile(int(bool(enable))))
+
+
+def attn_set_bwd_query_tile(rows: int):
+    """d = 64/128 backward: 128-row query tiles (dQ^T in dP^T's columns) or 64-row tiles
+    (dQ^T in columns of its own, next tile's products issued ahead)."""
+    _check(_lib.attn_set_bwd_query_tile(int(rows)))
 
 
 def attn_set_varlen_order(longest_first: bool = True):

@@ -48,6 +48,7 @@ std::atomic<int> g_test_skip_kv{0};
 std::atomic<int> g_varlen_lpt{1};
 std::atomic<int> g_one_tile_d128{0};
 std::atomic<int> g_persistent{0};
+std::atomic<int> g_bwd_tile_rows{128};   // d <= 128 backward: 128-row (bwd.cu) or 64-row (bwd_wide.cu) query tiles
 
 struct DevSyms {
   int* status = nullptr;
@@ -579,7 +580,16 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int determi
   if (check_shape(B, Hq, Hkv, N, d, 1.0f, true) != ATTN_OK) return (size_t)-1;
   if (B == 0 || N == 0) return 0;
   if (d > 128) return bwd_wide_workspace_bytes(B, Hq, N, d, deterministic);
-  return bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
+  // Enough for either query-tile choice (attn_set_bwd_query_tile), so that a workspace sized
+  // once serves both.
+  return std::max(bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic),
+                  bwd_wide_workspace_bytes(B, Hq, N, d, deterministic));
+}
+
+int attn_set_bwd_query_tile(int rows) {
+  if (rows != 64 && rows != 128) return fail(ATTN_ERR_INVALID_ARG, "query tile rows=%d (64 or 128)", rows);
+  g_bwd_tile_rows.store(rows);
+  return ATTN_OK;
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
@@ -588,7 +598,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   int rc = check_shape(B, Hq, Hkv, N, d, scale, true);
   if (rc != ATTN_OK) return rc;
   if (B == 0 || N == 0) return ATTN_OK;
-  const bool wide = d > 128;   // d = 192, 256: bwd_wide.cu
+  // 64-row query tiles (bwd_wide.cu): always for d = 192, 256; for d <= 128 when chosen.
+  const bool wide = d > 128 || g_bwd_tile_rows.load() == 64;
   const size_t need = wide ? bwd_wide_workspace_bytes(B, Hq, N, d, deterministic)
                            : bwd_workspace_bytes(B, Hq, Hkv, N, d, deterministic);
   if (!workspace || workspace_bytes < need)

@@ -1,27 +1,33 @@
-// Attention backward for wide heads, d = 192 and 256 ("Hotelren FA4 summary" section 6.2,
-// recommended head dims up to 256; the stages of section 4.2: S = K Q^T, dP = V dO^T,
-// dV = P^T dO, dS = P o (dP - D), dK = dS^T Q, dQ = dS K; the reverse-engineering page:
-// P is recomputed, never stored).
+// Attention backward with 64-row query tiles: d = 192 and 256, and the same design for d = 64
+// and 128 ("Hotelren FA4 summary" section 6.2, recommended head dims up to 256; the stages
+// of section 4.2: S = K Q^T, dP = V dO^T, dV = P^T dO, dS = P o (dP - D), dK = dS^T Q,
+// dQ = dS K; the reverse-engineering page: P is recomputed, never stored).
 //
-// Why a kernel of its own: at d = 256 the dV and dK accumulators of a 128-key block take
-// all 512 TMEM columns, and K, V, Q and dO tiles of 128 rows take 256 KB of shared memory.
-// So each CTA owns one 128-key block of one K/V head and one column half of dK, dV and dQ
-// (d = 256: columns 0-127 or 128-255; d = 192: columns 0-127 or 128-191), and walks query
-// tiles of 64 rows:
+// Each CTA owns one 128-key block of one K/V head and one column block of dK, dV and dQ,
+// and walks query tiles of 64 rows.  At d = 256 the dV and dK accumulators of a 128-key
+// block would take all 512 TMEM columns and K, V, Q and dO tiles of 128 rows 256 KB of
+// shared memory, so for d > 128 the columns are split in two halves over two CTAs (d = 256:
+// columns 0-127 and 128-255; d = 192: 0-127 and 128-191); for d <= 128 one CTA owns all of
+// them.
 //   S^T   = K Q^T           M = 128 keys, N = 64 queries, all d columns
 //   dP^T  = V dO^T          same shape
 //   P^T   = exp2(S^T c - LSE2)         (bf16 into the S^T columns)
-//   dV_h += P^T dO_h        N = the half's columns, A = P^T from TMEM
+//   dV_h += P^T dO_h        N = the block's columns, A = P^T from TMEM
 //   dS^T  = P^T o (dP^T - D)           (bf16 into shared memory)
 //   dK_h += dS^T Q_h
-//   dQ^T_h = K_h^T dS^T     M = the half's d rows (TMEM lane = dQ column), N = 64 queries
+//   dQ^T_h = K_h^T dS^T     M = the block's d rows (TMEM lane = dQ column), N = 64 queries
 //   dQacc += dQ_h           fp32 red.global.add, one 128-byte line of a row per warp
 //                           instruction (in key-block order when deterministic)
-// Both halves recompute S^T and dP^T (the price of the TMEM budget).  TMEM: S^T [0,64),
-// dP^T [64,128), dQ^T [128,192), dV_h, dK_h after (at most 448 columns).  dQ^T has columns
-// of its own, so the next tile's dP^T never waits for the drain.  Shared memory: K and V
-// tiles resident, Q and dO tiles of 64 rows in two stages (d = 192) or one (d = 256, where
-// a stage's dO is refilled after dV and its Q after dK), dS^T 16 KB.
+// Two halves both recompute S^T and dP^T (the price of the TMEM budget at d > 128).  TMEM:
+// S^T [0,64), dP^T [64,128), dQ^T [128,192), dV_h, dK_h after (at most 448 columns).  dQ^T
+// has columns of its own, so no product waits for the drain except the next dQ^T: the
+// loop-carried chain of the 128-row-tile kernel (dP^T -> dS^T -> dQ^T -> drain -> next dP^T,
+// with dQ^T aliasing dP^T) is gone.  Two threads issue the products: warp 1 dP^T, S^T and
+// dV, warp 2 dK and dQ^T (with 64-row tiles a product is short, and one thread's issue rate
+// would bound the tensor pipe).  Shared memory: K and V tiles resident; Q and dO tiles of
+// 64 rows in three stages (d <= 128), two (d = 192) or one (d = 256, where a stage's dO is
+// refilled after dV and its Q after dK); dS^T 16 KB.  With two or more stages the next
+// tile's S^T and dP^T are issued ahead of this tile's dK and dQ^T.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -45,7 +51,8 @@ struct BwCfg {
   static constexpr uint32_t KT = KCH * NCH;           // K or V tile, 128 x D
   static constexpr uint32_t QCH = 64 * 128;           // 64 rows x 64 bf16
   static constexpr uint32_t QT = QCH * NCH;           // Q or dO tile, 64 x D
-  static constexpr int NST = D == 192 ? 2 : 1;        // Q/dO stages
+  static constexpr int NHALF = D > 128 ? 2 : 1;       // column blocks of dK/dV/dQ (CTAs per key block)
+  static constexpr int NST = D == 256 ? 1 : (D == 192 ? 2 : 3);   // Q/dO stages
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = KT;
   static constexpr uint32_t OFF_Q = 2 * KT;                    // NST x QT
@@ -62,26 +69,27 @@ struct BwCfg {
 
 enum {
   X_KV = 0,
-  X_QFULL = 1,      // +stage
-  X_DOFULL = 3,     // +stage
-  X_QFREE = 5,      // +stage: dK (the stage's last Q reader) done
-  X_DOFREE = 7,     // +stage: dV (the stage's last dO reader) done
-  X_S = 9,          // S^T complete
-  X_DP = 10,        // dP^T complete
-  X_P = 11,         // P^T written (256)
-  X_DPFREE = 12,    // dP^T read by the compute warps (256)
-  X_DS = 13,        // dS^T written (256)
-  X_DSFREE = 14,    // dK and dQ^T (the readers of dS^T) done
-  X_DQ = 15,        // dQ^T complete
-  X_DQFREE = 16,    // dQ^T read by the drain (128)
-  X_VFULL = 17,     // vectors of the next tile written (32)
-  X_VFREE = 18,     // vectors read (256)
-  X_GD = 19,        // drain group barrier (128)
-  X_EPI = 20,       // epilogue staging written (128)
-  X_DONE = 21,
-  X_COUNT = 22
+  X_QFULL = 1,      // +stage (up to 3)
+  X_DOFULL = 4,     // +stage
+  X_QFREE = 7,      // +stage: dK (the stage's last Q reader) done
+  X_DOFREE = 10,    // +stage: dV (the stage's last dO reader) done
+  X_S = 13,         // S^T complete
+  X_DP = 14,        // dP^T complete
+  X_P = 15,         // P^T written (256)
+  X_DPFREE = 16,    // dP^T read by the compute warps (256)
+  X_DS = 17,        // dS^T written (256)
+  X_DSFREE = 18,    // dK and dQ^T (the readers of dS^T) done
+  X_DQ = 19,        // dQ^T complete
+  X_DQFREE = 20,    // dQ^T read by the drain (128)
+  X_VFULL = 21,     // vectors of the next tile written (32)
+  X_VFREE = 22,     // vectors read (256)
+  X_GD = 23,        // drain group barrier (128)
+  X_EPI = 24,       // epilogue staging written (128)
+  X_DONE = 25,
+  X_COUNT = 26
 };
 static_assert(X_COUNT * 8 + 8 <= 256, "barriers and the TMEM slot fit the control block");
+static_assert(BwCfg<64>::NST <= 3 && BwCfg<128>::NST <= 3, "three stage barriers of each kind");
 
 __device__ __forceinline__ bool w_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   const bool ok = mbar_wait(bar, parity, w);
@@ -129,7 +137,7 @@ struct BwArgs {
   const float* lse2;
   const float* delta;
   float* dq_acc;      // [B, Hq, nq64 * 64, D]
-  int* sem;           // [B, Hq, nq64, 2] when deterministic
+  int* sem;           // [B, Hq, nq64, column blocks] when deterministic
   unsigned long long wait_ns;
   int* status;
 };
@@ -155,14 +163,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   const int warp = warp_id(), lane = lane_id();
   // CTA -> (column half, key block, K/V head).  Causal grids launch key block 0 of every
   // head first (it sees the most query tiles); otherwise a head's blocks run together.
-  const int half = blockIdx.x & 1;
-  const int rest = blockIdx.x >> 1;
+  const int half = C::NHALF == 2 ? (int)(blockIdx.x & 1) : 0;
+  const int rest = C::NHALF == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int nbkv = a.B * a.Hkv;
   const int bkv = a.causal ? rest % nbkv : rest / a.nkb;
   const int n = a.causal ? rest / nbkv : rest % a.nkb;
   const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
   const int c0 = half * 128;                       // first dK/dV/dQ column of this CTA
-  const int DH = min(128, D - c0);                 // 128, or 64 for the second half at d = 192
+  const int DH = min(128, D - c0);                 // 128, or 64 (second half at d = 192; d = 64)
   const int m0 = a.causal ? 2 * n : 0;             // first 64-row query tile that sees the block
   const int n_m = a.nq64 - m0;
   const int n_iter = a.g * max(n_m, 0);
@@ -174,6 +182,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       if (i == X_P || i == X_DPFREE || i == X_DS || i == X_VFREE) cnt = 256;
       else if (i == X_DQFREE || i == X_GD || i == X_EPI) cnt = 128;
       else if (i == X_VFULL) cnt = 32;
+      else if (i == X_DONE) cnt = 2;      // one commit from each MMA-issuing thread
       mbar_init(BAR(i), cnt);
     }
     *abort_flag = 0;
@@ -247,18 +256,19 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         }
       }
     } else if (warp == 1) {
-      // -------------------------------------------------------------- MMA issuer
+      // -------------------------------------------------------------- first MMA issuer: dP^T, S^T, dV
       if (lane == 0) {
         bool ok = mbar_wait(BAR(X_KV), 0, wc);
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V, dsb = sbase + C::OFF_DS;
+        const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
         const uint32_t idesc_kv = idesc_bf16_f32(128, DH, false, true);
-        for (int it = 0; it < n_iter && ok; ++it) {
+        // dP^T = V dO^T for tile `it`, once its dO has landed and the compute warps have read
+        // the previous dP^T.
+        auto issue_dp = [&](int it) -> bool {
           const int st = it % C::NST;
-          const uint32_t qs = sbase + C::OFF_Q + st * C::QT, dos = sbase + C::OFF_DO + st * C::QT;
-          // dP^T = V dO^T, once the compute warps have read the previous dP^T
-          if (!mbar_wait(BAR(X_DOFULL + st), (it / C::NST) & 1, wc)) { ok = false; break; }
-          if (it > 0 && !mbar_wait(BAR(X_DPFREE), (it - 1) & 1, wc)) { ok = false; break; }
+          const uint32_t dos = sbase + C::OFF_DO + st * C::QT;
+          if (!mbar_wait(BAR(X_DOFULL + st), (it / C::NST) & 1, wc)) return false;
+          if (it > 0 && !mbar_wait(BAR(X_DPFREE), (it - 1) & 1, wc)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -266,8 +276,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             mma_ss(tdP, sdesc_sw128(vb + ka, 16, 1024), sdesc_sw128(dos + qa, 16, 1024), C::IDESC_S, kk > 0);
           }
           mma_commit(BAR(X_DP));
-          // S^T = K Q^T (the previous dV, which read P^T from these columns, was issued before)
-          if (!mbar_wait(BAR(X_QFULL + st), (it / C::NST) & 1, wc)) { ok = false; break; }
+          return true;
+        };
+        // S^T = K Q^T for tile `it` (the previous dV, which read P^T from these columns, was
+        // issued before it).
+        auto issue_s = [&](int it) -> bool {
+          const int st = it % C::NST;
+          const uint32_t qs = sbase + C::OFF_Q + st * C::QT;
+          if (!mbar_wait(BAR(X_QFULL + st), (it / C::NST) & 1, wc)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -275,6 +291,17 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             mma_ss(tS, sdesc_sw128(kb + ka, 16, 1024), sdesc_sw128(qs + qa, 16, 1024), C::IDESC_S, kk > 0);
           }
           mma_commit(BAR(X_S));
+          return true;
+        };
+        // With two or more stages the next tile's S^T and dP^T go ahead of this tile's dK
+        // and dQ^T, so that its probabilities and dS^T are computed while they run; with one
+        // stage (d = 256) the next tile's Q can only land after this tile's dK.
+        constexpr bool PIPE = C::NST >= 2;
+        if (PIPE && n_iter > 0) ok = ok && issue_dp(0) && issue_s(0);
+        for (int it = 0; it < n_iter && ok; ++it) {
+          const int st = it % C::NST;
+          const uint32_t dos = sbase + C::OFF_DO + st * C::QT;
+          if (!PIPE && !(issue_dp(it) && issue_s(it))) { ok = false; break; }
           // dV_h += P^T dO_h: P^T of queries 32 w .. 32 w + 31 sits in columns 32 w .. 32 w + 15.
           if (!mbar_wait(BAR(X_P), it & 1, wc)) { ok = false; break; }
           tc_fence_after();
@@ -283,6 +310,26 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8,
                    sdesc_sw128(dos + (c0 / 64) * C::QCH + kk * 2048, C::QCH, 1024), idesc_kv, (it > 0 || kk > 0));
           mma_commit(BAR(X_DOFREE + st));
+          if (PIPE && it + 1 < n_iter && !(issue_s(it + 1) && issue_dp(it + 1))) { ok = false; break; }
+        }
+        mma_commit(BAR(X_DONE));
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(BAR(X_DONE), 0) && globaltimer_ns() - t0 < a.wait_ns) {
+        }
+      }
+    } else if (warp == 2) {
+      // -------------------------------------------------------------- second MMA issuer: dK, dQ^T
+      // Its accumulators (dK, dQ^T) are disjoint from the first issuer's (S^T, dP^T, dV), and
+      // each thread's commits track only its own products, so the two streams only meet
+      // through the barriers below.
+      if (lane == 0) {
+        bool ok = mbar_wait(BAR(X_KV), 0, wc);
+        tc_fence_after();
+        const uint32_t kb = sbase + C::OFF_K, dsb = sbase + C::OFF_DS;
+        const uint32_t idesc_kv = idesc_bf16_f32(128, DH, false, true);
+        for (int it = 0; it < n_iter && ok; ++it) {
+          const int st = it % C::NST;
+          const uint32_t qs = sbase + C::OFF_Q + st * C::QT;
           // dK_h += dS^T Q_h
           if (!mbar_wait(BAR(X_DS), it & 1, wc)) { ok = false; break; }
           tc_fence_after();
@@ -500,7 +547,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       for (int it = 0; it < n_iter; ++it) {
         int bh, m;
         iter_head_row(it, bh, m);
-        int* sem = a.sem + ((size_t)bh * a.nq64 + m) * 2 + half;
+        int* sem = a.sem + ((size_t)bh * a.nq64 + m) * C::NHALF + half;
         if (leader) {
           const unsigned long long t0 = globaltimer_ns();
           while (w_ld_acquire(sem) != n) {
@@ -535,7 +582,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   }
 }
 
-// Preprocess for d = 192, 256: 16 threads per row; D = rowsum(dO o O), LSE2 = LSE log2(e),
+// Preprocess: 16 threads per row; D = rowsum(dO o O), LSE2 = LSE log2(e),
 // the row's dQacc zeroed (rows padded to whole 64-row tiles), counters zeroed.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_wide_preprocess_kernel(const uint16_t* __restrict__ o,
@@ -544,7 +591,7 @@ __global__ void __launch_bounds__(256) bwd_wide_preprocess_kernel(const uint16_t
                                                                    float* __restrict__ delta, float* __restrict__ lse2,
                                                                    float* __restrict__ dq_acc, int* __restrict__ sem,
                                                                    long long rows, int N, int npad, long long n_sem) {
-  constexpr int PER = D / 16;   // 12 or 16 elements per thread
+  constexpr int PER = D / 16;   // 4, 8, 12 or 16 elements per thread
   const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
   const int sub = threadIdx.x & 15;
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -598,7 +645,7 @@ template <int D, bool DET>
 cudaError_t launch_wide_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) {
   const long long rows = (long long)p.B * p.Hq * p.N;
   const int nq64 = (p.N + 63) / 64;
-  const long long n_sem = DET ? (long long)p.B * p.Hq * nq64 * 2 : 0;
+  const long long n_sem = DET ? (long long)p.B * p.Hq * nq64 * BwCfg<D>::NHALF : 0;
   {
     const long long blocks = std::max((rows + 15) / 16, (n_sem + 255) / 256);
     if (blocks > 0) {
@@ -628,7 +675,7 @@ cudaError_t launch_wide_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) 
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
-    const long long grid = (long long)p.B * p.Hkv * a.nkb * 2;
+    const long long grid = (long long)p.B * p.Hkv * a.nkb * BwCfg<D>::NHALF;
     if (grid > 0) {
       kern<<<(unsigned)grid, kBwThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
       e = cudaGetLastError();
@@ -650,7 +697,7 @@ size_t bwd_wide_workspace_bytes(int B, int Hq, int N, int d, int deterministic) 
   const size_t rows = (size_t)B * Hq * N;
   const size_t nq64 = (size_t)(N + 63) / 64;
   size_t n = al((size_t)B * Hq * nq64 * 64 * d * 4) + 2 * al(rows * 4);
-  if (deterministic) n += al((size_t)B * Hq * nq64 * 2 * 4);
+  if (deterministic) n += al((size_t)B * Hq * nq64 * (d > 128 ? 2 : 1) * 4);
   return n;
 }
 
@@ -669,6 +716,8 @@ void bwd_wide_workspace_carve(void* ws, int B, int Hq, int N, int d, int determi
 }
 
 cudaError_t launch_bwd_wide(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream) {
+  if (p.D == 64) return p.deterministic ? launch_wide_t<64, true>(maps, p, stream) : launch_wide_t<64, false>(maps, p, stream);
+  if (p.D == 128) return p.deterministic ? launch_wide_t<128, true>(maps, p, stream) : launch_wide_t<128, false>(maps, p, stream);
   if (p.D == 192) return p.deterministic ? launch_wide_t<192, true>(maps, p, stream) : launch_wide_t<192, false>(maps, p, stream);
   if (p.D == 256) return p.deterministic ? launch_wide_t<256, true>(maps, p, stream) : launch_wide_t<256, false>(maps, p, stream);
   return cudaErrorNotSupported;

@@ -287,8 +287,9 @@ def varlen_lines(A, torch, dev, flush):
 
 
 def wide_lines(A, torch, dev, flush):
-    """Forward-only lines for wide heads (the one-tile kernel): B=2, H=16, N=8192, d = 192
-    and 256, non-causal and causal.  FLOPs 4*B*H*N^2*d, halved for causal."""
+    """Lines for wide heads: B=2, H=16, N=8192, d = 192 and 256, non-causal and causal; the
+    forward (one-tile kernel, FLOPs 4*B*H*N^2*d, halved for causal) and the backward (the
+    column-half kernel, 2.5 times the forward FLOPs, atomic dQ)."""
     res = {}
     B, H, N = 2, 16, 8192
     for d in (192, 256):
@@ -296,6 +297,9 @@ def wide_lines(A, torch, dev, flush):
         q, k, v = (torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        do = torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty((A.attn_bwd_workspace_size(B, H, H, N, d, False),), dtype=torch.uint8, device=dev)
         for causal in (False, True):
             call = lambda: A.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, o=o, lse=lse)
             for _ in range(3):
@@ -309,9 +313,13 @@ def wide_lines(A, torch, dev, flush):
             torch.cuda.synchronize()
             ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
             tf = fwd_flops(B, H, N, d, causal) / ms / 1e9
+            msb = _median_ms(torch, flush, lambda: A.attn_bwd(q, k, v, o, lse, do, causal=causal, scale=d ** -0.5,
+                                                              dq=dq, dk=dk, dv=dv, workspace=ws))
+            tfb = 2.5 * fwd_flops(B, H, N, d, causal) / msb / 1e9
             res[f"d{d}_{'causal' if causal else 'noncausal'}"] = {
-                "ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_2250": round(tf / NOMINAL_PEAK_TFLOPS, 4)}
-        del q, k, v, o, lse
+                "ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_2250": round(tf / NOMINAL_PEAK_TFLOPS, 4),
+                "bwd_ms": round(msb, 4), "bwd_tflops": round(tfb, 1), "bwd_frac_of_2250": round(tfb / NOMINAL_PEAK_TFLOPS, 4)}
+        del q, k, v, o, lse, do, dq, dk, dv, ws
     if A.attn_device_status(True) != 0:
         raise RuntimeError("a kernel reported a timeout in the wide-head lines")
     return res
@@ -490,9 +498,11 @@ def _case_table():
             return lambda: A.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, o=o, lse=lse)
         return setup
 
-    def bwd(b, h, n, d, causal, det=False, seed=5):
+    def bwd(b, h, n, d, causal, det=False, seed=5, tile=None):
         def setup(A, torch, dev):
             from attn_inputs import make_inputs
+            if tile is not None:
+                A.attn_set_bwd_query_tile(tile)
             x = make_inputs(seed, b, h, h, n, d, with_grad=True)
             q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
             o, lse = A.attn_fwd(q, k, v, causal=causal)
@@ -551,6 +561,26 @@ def _case_table():
                                            fwd(2, 32, 8, 8192, 128, True, recipe="outliers", seed=4)),
         "bwd_train_B4_H16_N2048": ("backward B4 H16 N2048 d128 non-causal", bwd(4, 16, 2048, 128, False, seed=2)),
         "bwd_N8192_noncausal": ("backward B2 H16 N8192 d128 non-causal", bwd(2, 16, 8192, 128, False)),
+        "bwd_train_tile64": ("backward B4 H16 N2048 d128 non-causal, 64-row query tiles",
+                             bwd(4, 16, 2048, 128, False, seed=2, tile=64)),
+        "bwd_train_tile128": ("backward B4 H16 N2048 d128 non-causal, 128-row query tiles",
+                              bwd(4, 16, 2048, 128, False, seed=2, tile=128)),
+        "bwd_N8192_tile64": ("backward B2 H16 N8192 d128 non-causal, 64-row query tiles",
+                             bwd(2, 16, 8192, 128, False, tile=64)),
+        "bwd_N8192_causal_tile64": ("backward B2 H16 N8192 d128 causal, 64-row query tiles",
+                                    bwd(2, 16, 8192, 128, True, tile=64)),
+        "bwd_N8192_causal_tile128": ("backward B2 H16 N8192 d128 causal, 128-row query tiles",
+                                     bwd(2, 16, 8192, 128, True, tile=128)),
+        "bwd_N8192_det_tile64": ("backward B2 H16 N8192 d128 non-causal deterministic, 64-row query tiles",
+                                 bwd(2, 16, 8192, 128, False, det=True, tile=64)),
+        "bwd_d64_train_tile64": ("backward B4 H16 N2048 d64 non-causal, 64-row query tiles",
+                                 bwd(4, 16, 2048, 64, False, seed=2, tile=64)),
+        "bwd_d64_train_tile128": ("backward B4 H16 N2048 d64 non-causal, 128-row query tiles",
+                                  bwd(4, 16, 2048, 64, False, seed=2, tile=128)),
+        "bwd_d256_N8192_noncausal": ("backward B2 H16 N8192 d256 non-causal (column halves)",
+                                     bwd(2, 16, 8192, 256, False)),
+        "bwd_d192_N8192_noncausal": ("backward B2 H16 N8192 d192 non-causal (column halves)",
+                                     bwd(2, 16, 8192, 192, False)),
         "bwd_N8192_noncausal_det": ("same, deterministic dQ", bwd(2, 16, 8192, 128, False, det=True)),
         "varlen_fwd_noncausal": ("packed forward, 18 sequences (65536 tokens), H16 d128", varlen(False, False)),
         "varlen_bwd_noncausal": ("packed backward, same batch", varlen(True, False)),

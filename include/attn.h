@@ -208,6 +208,17 @@ int attn_set_fwd_persistent(int enable);
 int attn_set_fwd_one_tile(int enable);
 
 /*
+ * Query tile of attn_bwd (and attn_bwd_noalloc) for d = 64 and 128: 128 = one 128-key block
+ * per CTA walking 128-row query tiles, dQ^T formed in the columns of dP^T (bwd.cu); 64 =
+ * 64-row query tiles with dQ^T in tensor-memory columns of its own and the next tile's
+ * products issued ahead of this tile's dK and dQ^T (bwd_wide.cu, the kernel that always
+ * serves d = 192 and 256).  Same results within the backward's error bounds (the order of
+ * the fp32 dQ additions differs).  attn_bwd_workspace_size covers both.  A tuning knob,
+ * process-wide; ATTN_ERR_INVALID_ARG for other values.
+ */
+int attn_set_bwd_query_tile(int rows);
+
+/*
  * Order of attn_fwd_varlen's tiles and attn_bwd_varlen's key blocks: 1 (default) = the
  * CTAs with the most work first; 0 = no ordering (the order in which the scheduler meets
  * the sequences).  The results are the same either way; the knob exists to measure what
