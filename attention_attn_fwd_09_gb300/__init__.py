@@ -45,6 +45,8 @@ _lib.attn_set_fwd_persistent.argtypes = [_i]
 _lib.attn_set_fwd_persistent.restype = _i
 _lib.attn_set_fwd_one_tile.argtypes = [_i]
 _lib.attn_set_fwd_one_tile.restype = _i
+_lib.attn_set_decode_one_tile.argtypes = [_i]
+_lib.attn_set_decode_one_tile.restype = _i
 _lib.attn_set_bwd_query_tile.argtypes = [_i]
 _lib.attn_set_bwd_query_tile.restype = _i
 _lib.attn_set_varlen_order.argtypes = [_i]
@@ -298,6 +300,12 @@ def attn_set_fwd_persistent(enable: bool):
 def attn_set_fwd_one_tile(enable: bool):
     """d = 128 forward kernel: one query tile per CTA (True) or two (False)."""
     _check(_lib.attn_set_fwd_one_tile(int(bool(enable))))
+
+
+def attn_set_decode_one_tile(enable: bool):
+    """attn_fwd_kv grouped decode at d = 128: the one-tile kernel (True, default) or the
+    two-tile kernel (False)."""
+    _check(_lib.attn_set_decode_one_tile(int(bool(enable))))
 
 
 def attn_set_bwd_query_tile(rows: int):

@@ -48,6 +48,7 @@ std::atomic<int> g_test_skip_kv{0};
 std::atomic<int> g_varlen_lpt{1};
 std::atomic<int> g_one_tile_d128{0};
 std::atomic<int> g_persistent{0};
+std::atomic<int> g_decode_one_tile{1};    // grouped decode at d = 128 through the one-tile kernel (fwd_wide.cu)
 std::atomic<int> g_bwd_tile_rows{128};   // d <= 128 backward: 128-row (bwd.cu) or 64-row (bwd_wide.cu) query tiles
 
 struct DevSyms {
@@ -345,8 +346,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Persistent two-tile kernel (fwd_persist.cu): one CTA per SM walking the same work list.
   const bool persist = !wide && !pack && g_persistent.load() && g_poly.load() == 0;
+  // Grouped decode at d = 128: the one-tile kernel (S of the next key block overlaps the
+  // softmax of this one) unless the two-tile kernel is chosen.
+  const bool pack_one_tile = pack && d == 128 && g_decode_one_tile.load();
   cudaError_t e;
-  if (persist) {
+  if (pack_one_tile) {
+    e = launch_fwd_wide(maps, p, d, (int)grid, st);
+  } else if (persist) {
     p.o_ptr = o;
     const long long entries = grid;
     const long long pgrid = std::min<long long>(entries, std::max(1, s->sms));
@@ -403,6 +409,11 @@ size_t attn_fwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d
 
 int attn_set_fwd_persistent(int enable) {
   g_persistent.store(enable ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_set_decode_one_tile(int enable) {
+  g_decode_one_tile.store(enable ? 1 : 0);
   return ATTN_OK;
 }
 

@@ -14,6 +14,11 @@
 // another).  TMEM: S buffers [0,128) and [128,256) (P overwrites the first 64 columns of
 // its buffer as bf16 pairs), O [256, 256+d).
 //
+// The same kernel serves d = 128 when one query tile per CTA is chosen, and grouped decode at
+// d = 128 (the group's query heads x a few queries in one tile, keys split over CTAs): there a
+// CTA has only one tile anyway, and the overlap of S_(j+1) with the softmax of block j is what
+// keeps the tensor core busy.
+//
 // Warp roles: warp 0 TMA producer (Q once, K and V tiles through a ring), warp 1 MMA
 // issuer, warp 2 TMEM allocator, warpgroup 1 softmax (one row per thread), warpgroups 2
 // and 3 correction and epilogue (each owns half of O's columns: the conditional rescale
@@ -106,6 +111,7 @@ __device__ __forceinline__ bool item_at(int pos, int n, int& j) {
 struct WideTile {
   int n, row0, bh, bkv;
   int qs, qend, krow0, nk, koff;
+  int j0;         // first key block (grouped decode: the start of this CTA's key split)
 };
 __device__ __forceinline__ WideTile map_wide(const FwdParams& p, int cta) {
   WideTile T;
@@ -123,6 +129,22 @@ __device__ __forceinline__ WideTile map_wide(const FwdParams& p, int cta) {
   T.bkv = b * p.Hkv + hq / p.g;
   T.n = p.causal ? (min(T.row0 + 127, p.N - 1) + p.koff) / 128 + 1 : p.n_kvblk;
   T.qs = 0; T.qend = p.N; T.krow0 = 0; T.nk = p.Nk; T.koff = p.koff;
+  T.j0 = 0;
+  return T;
+}
+
+// Grouped decode (d = 128): CTA = (K/V head, key split); its tile holds the group's g query
+// heads x N queries as rows h * N + q (rows past g * N are padding and never written).
+__device__ __forceinline__ WideTile map_wide_grouped(const FwdParams& p, int cta) {
+  WideTile T;
+  const int unit = cta / p.kv_splits, sp = cta % p.kv_splits;
+  const int b = unit / p.Hkv, hkv = unit % p.Hkv;
+  T.bkv = unit;
+  T.bh = b * p.Hq + hkv * p.g;
+  T.row0 = 0;
+  T.j0 = sp * p.blocks_per_split;
+  T.n = min(p.n_kvblk, T.j0 + p.blocks_per_split) - T.j0;
+  T.qs = 0; T.qend = p.N; T.krow0 = 0; T.nk = p.Nk; T.koff = p.koff;
   return T;
 }
 
@@ -138,16 +160,22 @@ __device__ __forceinline__ WideTile map_wide_varlen(const FwdParams& p, const in
   T.bh = hq;
   T.bkv = hq / p.g;
   T.n = p.causal ? (min(r0 + 127, nq - 1) + T.koff) / 128 + 1 : (nk + 127) / 128;
+  T.j0 = 0;
   return T;
 }
 
-// VL: packed variable-length sequences (d = 192, 256): one unit-table record per CTA.
-template <int D, bool VL>
+// MODE 0: the standard forward; MODE 1: grouped decode (d = 128; partial results to the
+// workspace, merged by launch_fwd_merge); MODE 2: packed variable-length sequences (d = 192,
+// 256; one unit-table record per CTA).
+template <int D, int MODE>
 __global__ void __launch_bounds__(kWideThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                          const FwdParams p) {
   using C = WideCfg<D>;
+  constexpr bool VL = MODE == 2;
+  constexpr bool GRP = MODE == 1;
+  static_assert(!GRP || C::SPLIT, "grouped decode through the one-tile kernel at d = 128 only");
   static_assert(V_FULL + C::NS <= V_SFULL, "every ring slot needs its own barrier below the next group");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,6 +199,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // tensor memory.
     if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
     T = map_wide_varlen(p, p.vl_units[blockIdx.x]);
+  } else if constexpr (GRP) {
+    T = map_wide_grouped(p, blockIdx.x);
   } else {
     T = map_wide(p, blockIdx.x);
   }
@@ -216,7 +246,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      mbar_arrive_expect_tx(BAR(V_Q), C::TILE);
+      mbar_arrive_expect_tx(BAR(V_Q), GRP ? p.q_tile_bytes : C::TILE);
       for (int c = 0; c < C::NCH; ++c) tma_load_3d(sbase + C::OFF_Q + c * C::CHUNK, &tm_q, c * 64, T.row0, T.bh, BAR(V_Q));
       // A slot is refilled once its previous occupant's reader completed: S_i for K_i,
       // PV_i for V_i.
@@ -239,8 +269,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_arrive_expect_tx(BAR(V_FULL + slot), C::TILE);
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, T.krow0 + j * 128, T.bkv,
-                      BAR(V_FULL + slot));
+          tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, T.krow0 + (T.j0 + j) * 128,
+                      T.bkv, BAR(V_FULL + slot));
       }
       if (!ok) {
         // Let the copies still in flight land before the CTA's shared memory goes away.
@@ -328,10 +358,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tmem_wait_ld();
       reg_fence_w(u);
       float* s = reinterpret_cast<float*>(u);
-      const int kb = j * 128 + h * 64;
-      const bool need_mask = (kb + 63 >= T.nk) || (p.causal && kb + 63 > T.row0 - T.qs + T.koff);
+      const int kb = (T.j0 + j) * 128 + h * 64;
+      // Grouped decode: row = hq * N + q holds query q (rows past g * N are padding).
+      const int qrow = GRP ? row % p.N : grow - T.qs;
+      const bool need_mask = GRP || (kb + 63 >= T.nk) || (p.causal && kb + 63 > T.row0 - T.qs + T.koff);
       if (need_mask) {
-        const int lim = (p.causal ? min(grow - T.qs + T.koff, T.nk - 1) : T.nk - 1) - kb;   // last visible column
+        const int lim = (p.causal ? min(qrow + T.koff, T.nk - 1) : T.nk - 1) - kb;   // last visible column
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -365,7 +397,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         alpha_buf[(j & 1) * 128 + row] = alpha;
         mbar_arrive(BAR(V_STATS + (j & 1)));
       }
-      const float neg_m = -m;
+      // Grouped decode: a row may see no key of this CTA's split yet (m = -inf); its
+      // probabilities are then 0, not 2^(-inf + inf).
+      const float neg_m = (GRP && m == -INFINITY) ? 0.f : -m;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
@@ -520,7 +554,34 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     // Epilogue: O / lq -> bf16 -> swizzled shared memory (the Q tile, free once the last
     // S product completed, which it did before the last PV) -> TMA store; LSE to global.
-    if (ok && n > 0 && warp_wait_w(BAR(V_FIN), 0, wc) &&
+    // Grouped decode: this key split's partial result, O / lq (0 where the row saw no key)
+    // and LSE in fp32, for rows h * N + q of the group, to the workspace.
+    if (GRP && ok && n > 0 && warp_wait_w(BAR(V_FIN), 0, wc) &&
+        warp_wait_w(BAR(V_PVD + ((n - 1) & 1)), ((n - 1) >> 1) & 1, wc)) {
+      tc_fence_after();
+      const int unit = blockIdx.x / p.kv_splits, sp = blockIdx.x % p.kv_splits;
+      const size_t slot = (size_t)sp * (p.B * p.Hkv) + unit;
+      const bool real = row < p.g * p.N;
+      const float lrow = l_fin[row] + l_fin[128 + row];
+      const float lqr = lq_fin[row] + lq_fin[128 + row];
+      const float invp = lqr > 0.f ? 1.f / lqr : 0.f;
+      float* dst = p.part_o + (slot * 128 + row) * D;
+      uint32_t r[32];
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {
+        tmem_ld32(tO + q * 32, r);   // warp-collective: every lane loads its row
+        tmem_wait_ld();
+        reg_fence_w(r);
+        if (real) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + q * 32 + i) =
+                make_float4(__uint_as_float(r[i]) * invp, __uint_as_float(r[i + 1]) * invp,
+                            __uint_as_float(r[i + 2]) * invp, __uint_as_float(r[i + 3]) * invp);
+        }
+      }
+      if (real) p.part_lse[slot * 128 + row] = lrow > 0.f ? (m_fin[row] + __log2f(lrow)) * kLn2 : -INFINITY;
+    } else if (!GRP && ok && n > 0 && warp_wait_w(BAR(V_FIN), 0, wc) &&
         warp_wait_w(BAR(V_PVD + ((n - 1) & 1)), ((n - 1) >> 1) & 1, wc)) {
       tc_fence_after();
       const float lrow = C::SPLIT ? l_fin[row] + l_fin[128 + row] : l_fin[row];
@@ -581,9 +642,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-template <int D, bool VL>
+template <int D, int MODE>
 cudaError_t launch_wide_t(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
-  auto kern = attn_fwd_wide_kernel<D, VL>;
+  auto kern = attn_fwd_wide_kernel<D, MODE>;
   constexpr uint32_t smem = WideCfg<D>::SMEM;
   static std::once_flag flags[64];
   static cudaError_t attr_err[64];
@@ -602,13 +663,17 @@ cudaError_t launch_wide_t(const FwdMaps& m, const FwdParams& p, int grid, cudaSt
 
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t s) {
   if (p.pack == 2) {   // packed sequences (d = 192, 256)
-    if (D == 192) return launch_wide_t<192, true>(maps, p, grid, s);
-    if (D == 256) return launch_wide_t<256, true>(maps, p, grid, s);
+    if (D == 192) return launch_wide_t<192, 2>(maps, p, grid, s);
+    if (D == 256) return launch_wide_t<256, 2>(maps, p, grid, s);
     return cudaErrorInvalidValue;
   }
-  if (D == 128) return launch_wide_t<128, false>(maps, p, grid, s);
-  if (D == 192) return launch_wide_t<192, false>(maps, p, grid, s);
-  if (D == 256) return launch_wide_t<256, false>(maps, p, grid, s);
+  if (p.pack == 1) {   // grouped decode (d = 128)
+    if (D == 128) return launch_wide_t<128, 1>(maps, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
+  if (D == 128) return launch_wide_t<128, 0>(maps, p, grid, s);
+  if (D == 192) return launch_wide_t<192, 0>(maps, p, grid, s);
+  if (D == 256) return launch_wide_t<256, 0>(maps, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

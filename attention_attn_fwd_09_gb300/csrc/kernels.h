@@ -83,7 +83,9 @@ size_t fwd_smem_bytes(int D);
 cudaError_t launch_fwd_persistent(const FwdMaps& maps, const FwdParams& p, int D, int grid, int n_entries,
                                   cudaStream_t stream);
 // One-tile forward (fwd_wide.cu) for d = 128, 192 or 256: one 128-row query tile per CTA,
-// grid = B * Hq * ceil(N / 128); same parameters as launch_fwd (ordinary mode only).
+// grid = B * Hq * ceil(N / 128); same parameters as launch_fwd.  pack == 1 (grouped decode,
+// d = 128: grid = B * Hkv * kv_splits, then launch_fwd_merge) and pack == 2 (packed
+// sequences, d = 192, 256: grid = the table's bound) as for launch_fwd.
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, int D, int grid, cudaStream_t stream);
 
 // FP8 forward (fwd_fp8.cu), d = 128, ordinary tiling: Q/K/V maps over e4m3 bytes (boxes

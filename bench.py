@@ -535,9 +535,10 @@ def _case_table():
             return lambda: A.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal, o=o, lse=lse)
         return setup
 
-    def decode(nq):
+    def decode(nq, one_tile=True):
         def setup(A, torch, dev):
             from attn_inputs import make_inputs
+            A.attn_set_decode_one_tile(one_tile)
             B, Hq, Hkv, Nk, d = 8, 32, 8, 8192, 128
             x = make_inputs(6, B, Hq, Hkv, Nk, d)
             k, v = x["k"].to(dev), x["v"].to(dev)
@@ -588,6 +589,8 @@ def _case_table():
         "fp8_fwd_N4096_noncausal": ("FP8 forward B4 H16 N4096 d128 non-causal", fwd_fp8(4, 4096, False)),
         "decode_Nq1": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 1 query", decode(1)),
         "decode_Nq16": ("grouped decode B8 Hq32 Hkv8 Nk8192 d128, 16 queries", decode(16)),
+        "decode_Nq1_two_tile": ("same, 1 query, two-tile kernel", decode(1, False)),
+        "decode_Nq16_two_tile": ("same, 16 queries, two-tile kernel", decode(16, False)),
     }
 
 
@@ -612,6 +615,7 @@ def run_case(args):
         e[1].record()
     torch.cuda.synchronize()
     A.attn_set_debug_knobs()
+    A.attn_set_decode_one_tile(True)
     if A.attn_device_status(True) != 0:
         raise RuntimeError("a kernel reported a timeout")
     return {"case": args.case, "what": desc, "steps": args.steps, "warmup": args.warmup,

@@ -219,6 +219,15 @@ int attn_set_fwd_one_tile(int enable);
 int attn_set_bwd_query_tile(int rows);
 
 /*
+ * Which kernel serves attn_fwd_kv's grouped decode (g * Nq <= 128) at d = 128: 1 (default) =
+ * the one-tile kernel (fwd_wide.cu), in which S of the next key block overlaps the softmax of
+ * the current one; 0 = the two-tile kernel with its second tile slot empty (fwd.cu).  Same
+ * results up to the order of the rounding; d = 64 always uses the two-tile kernel.  A tuning
+ * knob, process-wide.
+ */
+int attn_set_decode_one_tile(int enable);
+
+/*
  * Order of attn_fwd_varlen's tiles and attn_bwd_varlen's key blocks: 1 (default) = the
  * CTAs with the most work first; 0 = no ordering (the order in which the scheduler meets
  * the sequences).  The results are the same either way; the knob exists to measure what

@@ -80,3 +80,27 @@ def test_grouped_decode_matches_ordinary_tiling(A, causal):
     assert A.attn_device_status(True) == 0
     assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
     assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+GROUPED = [s for s in SHAPES if s[2] < s[1] and s[1] // s[2] * s[3] <= 128]
+
+
+@pytest.mark.parametrize("shape", GROUPED, ids=lambda s: "B%dHq%dHkv%dNq%dNk%dd%d" % s)
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_decode_two_tile_kernel(A, shape, causal):
+    # The grouped decode through the two-tile kernel (the one-tile kernel serves d = 128 by
+    # default; d = 64 always takes this path) against the oracle.
+    B, Hq, Hkv, Nq, Nk, d = shape
+    x = make_inputs(500 + Nq + Nk + d, B, Hq, Hkv, Nk, d)
+    q = x["q"][:, :, Nk - Nq:].contiguous()
+    scale = default_scale(d)
+    dev = torch.device("cuda")
+    A.attn_set_decode_one_tile(False)
+    try:
+        o, lse = A.attn_fwd_kv(q.to(dev), x["k"].to(dev), x["v"].to(dev), causal=causal, scale=scale)
+        torch.cuda.synchronize()
+    finally:
+        A.attn_set_decode_one_tile(True)
+    assert A.attn_device_status(True) == 0
+    O, L = oracle.attn_fwd_kv(q, x["k"], x["v"], causal, scale)
+    check_fwd(o.float().cpu().numpy(), lse.cpu().numpy(), O, L, f"two-tile {shape} causal={causal}")
