@@ -338,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < nmax && !mbar_wait(BAR(B_FULL + kslot), (kidx / C::NS) & 1, wc)) { ok = false; break; }
         if (j >= 1 && !mbar_wait(BAR(B_FULL + vslot), (vidx / C::NS) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kbase = sbase + C::OFF_RING + kslot * C::TILE;
-        const uint32_t vbase = sbase + C::OFF_RING + vslot * C::TILE;
+        // Descriptor low words built once per block and advanced by (offset / 16); the high
+        // words are constants.
+        const uint32_t klo = sdesc_sw128_lo(sbase + C::OFF_RING + kslot * C::TILE, 16);
+        const uint32_t vlo = sdesc_sw128_lo(sbase + C::OFF_RING + vslot * C::TILE, C::CHUNK);
+        constexpr uint32_t HI = sdesc_sw128_hi(1024);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -353,10 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024);
-              mma_ts(tO, tS + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts_w(tO, tS + kk * 8, vlo + kk * (2048 >> 4), HI, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
             // Only the tile's last PV is signalled here (for the epilogue).  The correction
             // group learns that PV_t(j-1) finished from S_t(j)'s completion instead: MMAs
             // complete in issue order.
@@ -364,12 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j < T.n[t]) {
             // S_t = Q_t K_j^T
-            const uint32_t qbase = sbase + C::OFF_Q + t * C::TILE;
+            const uint32_t qlo = sdesc_sw128_lo(sbase + C::OFF_Q + t * C::TILE, 16);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tS, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
-                     kk > 0 ? 1u : 0u);
+              const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+              mma_ss_w(tS, qlo + off, HI, klo + off, HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(B_SFULL + t));
           }
