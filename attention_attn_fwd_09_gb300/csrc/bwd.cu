@@ -432,17 +432,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       bool ok = mbar_wait(BAR(W_KV), 0, wc);
       tc_fence_after();
-      const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V, dsb = sbase + C::OFF_DS;
+      // Matrix descriptors as low words (start address and leading byte offset) advanced by
+      // (offset / 16), with one constant high word: one add per operand per MMA.
+      constexpr uint32_t HI = sdesc_sw128_hi(1024);
+      const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_K, 16);            // K, K-major
+      const uint32_t kt_lo = sdesc_sw128_lo(sbase + C::OFF_K, C::CHUNK);     // K^T, MN-major
+      const uint32_t v_lo = sdesc_sw128_lo(sbase + C::OFF_V, 16);
+      const uint32_t ds_lo = sdesc_sw128_lo(sbase + C::OFF_DS, 16);          // dS^T, K-major
+      const uint32_t dst_lo = sdesc_sw128_lo(sbase + C::OFF_DS, C::CHUNK);   // dS^T, MN-major
       // S^T = K Q^T for tile `it`, once its Q/dO stage has landed.
       auto issue_s = [&](int it) -> bool {
         const int st = it & 1;
         if (!mbar_wait(BAR(W_FULL + st), (it >> 1) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t qs = sbase + C::OFF_STAGE + st * 2 * C::TILE;
+        const uint32_t q_lo = sdesc_sw128_lo(sbase + C::OFF_STAGE + st * 2 * C::TILE, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024), C::IDESC_S, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          if constexpr (DET) {
+            const uint32_t a = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+            mma_ss(tS, sdesc_sw128(sbase + C::OFF_K + a, 16, 1024),
+                   sdesc_sw128(sbase + C::OFF_STAGE + st * 2 * C::TILE + a, 16, 1024), C::IDESC_S, kk > 0);
+          } else {
+            mma_ss_w(tS, k_lo + off, HI, q_lo + off, HI, C::IDESC_S, kk > 0);
+          }
         }
         mma_commit(BAR(W_S));
         return true;
@@ -454,10 +467,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dP^T = V dO^T, once the previous dQ^T has left those columns
         if (it > 0 && !mbar_wait(BAR(W_DQFREE), (it - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t do_lo = sdesc_sw128_lo(dos, 16), dot_lo = sdesc_sw128_lo(dos, C::CHUNK);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(tdP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dos + off, 16, 1024), C::IDESC_S, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          if constexpr (DET) {
+            const uint32_t a = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+            mma_ss(tdP, sdesc_sw128(sbase + C::OFF_V + a, 16, 1024), sdesc_sw128(dos + a, 16, 1024), C::IDESC_S, kk > 0);
+          } else {
+            mma_ss_w(tdP, v_lo + off, HI, do_lo + off, HI, C::IDESC_S, kk > 0);
+          }
         }
         mma_commit(BAR(W_DP));
         // dV += P^T dO
@@ -465,8 +484,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dos + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
-                 (it > 0 || kk > 0));
+          if constexpr (DET)
+            mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dos + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
+                   (it > 0 || kk > 0));
+          else
+            mma_ts_w(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, dot_lo + kk * (2048 >> 4), HI, C::IDESC_KB,
+                     (it > 0 || kk > 0));
         // The next tile's S^T goes ahead of this tile's dK and dQ, so that its
         // probabilities are computed while they run.  MMAs of one thread execute in issue
         // order: S^T lands in the columns of P^T only after dV has read them.
@@ -474,17 +497,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dK += dS^T Q ; dQ^T = K^T dS^T
         if (!mbar_wait(BAR(W_DS), it & 1, wc)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t qt_lo = sdesc_sw128_lo(qs, C::CHUNK);   // Q, MN-major
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(tdK, sdesc_sw128(dsb + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::CHUNK, 1024), C::IDESC_KB,
-                 (it > 0 || kk > 0));
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          if constexpr (DET)
+            mma_ss(tdK, sdesc_sw128(sbase + C::OFF_DS + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024),
+                   sdesc_sw128(qs + kk * 2048, C::CHUNK, 1024), C::IDESC_KB, (it > 0 || kk > 0));
+          else
+            mma_ss_w(tdK, ds_lo + off, HI, qt_lo + kk * (2048 >> 4), HI, C::IDESC_KB, (it > 0 || kk > 0));
         }
         mma_commit(BAR(W_EMPTY + st));  // dK was the stage's last reader: the producer may refill it
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tdP, sdesc_sw128(kb + kk * 2048, C::CHUNK, 1024), sdesc_sw128(dsb + kk * 2048, C::CHUNK, 1024),
-                 C::IDESC_DQT, kk > 0);
+          if constexpr (DET)
+            mma_ss(tdP, sdesc_sw128(sbase + C::OFF_K + kk * 2048, C::CHUNK, 1024),
+                   sdesc_sw128(sbase + C::OFF_DS + kk * 2048, C::CHUNK, 1024), C::IDESC_DQT, kk > 0);
+          else
+            mma_ss_w(tdP, kt_lo + kk * (2048 >> 4), HI, dst_lo + kk * (2048 >> 4), HI, C::IDESC_DQT, kk > 0);
         mma_commit(BAR(W_DQ));
         mma_commit(BAR(W_DSFREE));
       }

@@ -260,20 +260,21 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       if (lane == 0) {
         bool ok = mbar_wait(BAR(X_KV), 0, wc);
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
+        constexpr uint32_t HI = sdesc_sw128_hi(1024);
+        const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_K, 16), v_lo = sdesc_sw128_lo(sbase + C::OFF_V, 16);
         const uint32_t idesc_kv = idesc_bf16_f32(128, DH, false, true);
         // dP^T = V dO^T for tile `it`, once its dO has landed and the compute warps have read
         // the previous dP^T.
         auto issue_dp = [&](int it) -> bool {
           const int st = it % C::NST;
-          const uint32_t dos = sbase + C::OFF_DO + st * C::QT;
+          const uint32_t do_lo = sdesc_sw128_lo(sbase + C::OFF_DO + st * C::QT, 16);
           if (!mbar_wait(BAR(X_DOFULL + st), (it / C::NST) & 1, wc)) return false;
           if (it > 0 && !mbar_wait(BAR(X_DPFREE), (it - 1) & 1, wc)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::KCH + (kk & 3) * 32, qa = (kk >> 2) * C::QCH + (kk & 3) * 32;
-            mma_ss(tdP, sdesc_sw128(vb + ka, 16, 1024), sdesc_sw128(dos + qa, 16, 1024), C::IDESC_S, kk > 0);
+            const uint32_t ka = ((kk >> 2) * C::KCH + (kk & 3) * 32) >> 4, qa = ((kk >> 2) * C::QCH + (kk & 3) * 32) >> 4;
+            mma_ss_w(tdP, v_lo + ka, HI, do_lo + qa, HI, C::IDESC_S, kk > 0);
           }
           mma_commit(BAR(X_DP));
           return true;
@@ -282,13 +283,13 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         // issued before it).
         auto issue_s = [&](int it) -> bool {
           const int st = it % C::NST;
-          const uint32_t qs = sbase + C::OFF_Q + st * C::QT;
+          const uint32_t q_lo = sdesc_sw128_lo(sbase + C::OFF_Q + st * C::QT, 16);
           if (!mbar_wait(BAR(X_QFULL + st), (it / C::NST) & 1, wc)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::KCH + (kk & 3) * 32, qa = (kk >> 2) * C::QCH + (kk & 3) * 32;
-            mma_ss(tS, sdesc_sw128(kb + ka, 16, 1024), sdesc_sw128(qs + qa, 16, 1024), C::IDESC_S, kk > 0);
+            const uint32_t ka = ((kk >> 2) * C::KCH + (kk & 3) * 32) >> 4, qa = ((kk >> 2) * C::QCH + (kk & 3) * 32) >> 4;
+            mma_ss_w(tS, k_lo + ka, HI, q_lo + qa, HI, C::IDESC_S, kk > 0);
           }
           mma_commit(BAR(X_S));
           return true;
@@ -300,15 +301,15 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         if (PIPE && n_iter > 0) ok = ok && issue_dp(0) && issue_s(0);
         for (int it = 0; it < n_iter && ok; ++it) {
           const int st = it % C::NST;
-          const uint32_t dos = sbase + C::OFF_DO + st * C::QT;
+          const uint32_t dot_lo = sdesc_sw128_lo(sbase + C::OFF_DO + st * C::QT + (c0 / 64) * C::QCH, C::QCH);
           if (!PIPE && !(issue_dp(it) && issue_s(it))) { ok = false; break; }
           // dV_h += P^T dO_h: P^T of queries 32 w .. 32 w + 31 sits in columns 32 w .. 32 w + 15.
           if (!mbar_wait(BAR(X_P), it & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8,
-                   sdesc_sw128(dos + (c0 / 64) * C::QCH + kk * 2048, C::QCH, 1024), idesc_kv, (it > 0 || kk > 0));
+            mma_ts_w(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8, dot_lo + kk * (2048 >> 4), HI, idesc_kv,
+                     (it > 0 || kk > 0));
           mma_commit(BAR(X_DOFREE + st));
           if (PIPE && it + 1 < n_iter && !(issue_s(it + 1) && issue_dp(it + 1))) { ok = false; break; }
         }
@@ -325,26 +326,27 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       if (lane == 0) {
         bool ok = mbar_wait(BAR(X_KV), 0, wc);
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K, dsb = sbase + C::OFF_DS;
+        constexpr uint32_t HI = sdesc_sw128_hi(1024);
+        const uint32_t kt_lo = sdesc_sw128_lo(sbase + C::OFF_K + (c0 / 64) * C::KCH, C::KCH);   // K_h^T, MN-major
+        const uint32_t ds_lo = sdesc_sw128_lo(sbase + C::OFF_DS, 16);                           // dS^T, K-major
+        const uint32_t dst_lo = sdesc_sw128_lo(sbase + C::OFF_DS, 16);                          // dS^T, MN-major
         const uint32_t idesc_kv = idesc_bf16_f32(128, DH, false, true);
         for (int it = 0; it < n_iter && ok; ++it) {
           const int st = it % C::NST;
-          const uint32_t qs = sbase + C::OFF_Q + st * C::QT;
+          const uint32_t qt_lo = sdesc_sw128_lo(sbase + C::OFF_Q + st * C::QT + (c0 / 64) * C::QCH, C::QCH);
           // dK_h += dS^T Q_h
           if (!mbar_wait(BAR(X_DS), it & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tdK, sdesc_sw128(dsb + kk * 32, 16, 1024),
-                   sdesc_sw128(qs + (c0 / 64) * C::QCH + kk * 2048, C::QCH, 1024), idesc_kv, (it > 0 || kk > 0));
+            mma_ss_w(tdK, ds_lo + kk * (32 >> 4), HI, qt_lo + kk * (2048 >> 4), HI, idesc_kv, (it > 0 || kk > 0));
           mma_commit(BAR(X_QFREE + st));
           // dQ^T_h = K_h^T dS^T into columns of its own, once the drain has read the last one
           if (it > 0 && !mbar_wait(BAR(X_DQFREE), (it - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tdQ, sdesc_sw128(kb + (c0 / 64) * C::KCH + kk * 2048, C::KCH, 1024),
-                   sdesc_sw128(dsb + kk * 2048, 16, 1024), C::IDESC_DQT, kk > 0);
+            mma_ss_w(tdQ, kt_lo + kk * (2048 >> 4), HI, dst_lo + kk * (2048 >> 4), HI, C::IDESC_DQT, kk > 0);
           mma_commit(BAR(X_DQ));
           mma_commit(BAR(X_DSFREE));
         }

@@ -301,8 +301,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           if (j < nmax && !mbar_wait(BAR(E_KFULL + ks), (j / C::NK) & 1, wc)) { ok = false; break; }
           if (j >= 1 && !mbar_wait(BAR(E_V16FULL + vs), ((j - 1) / C::NV16) & 1, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kbase = sbase + C::OFF_K + ks * C::T8;
-          const uint32_t vbase = sbase + C::OFF_V16 + vs * C::T16;
+          constexpr uint32_t HI = sdesc_sw128_hi(1024);
+          const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_K + ks * C::T8, 16);
+          const uint32_t v_lo = sdesc_sw128_lo(sbase + C::OFF_V16 + vs * C::T16, C::CH16);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!ok) break;
@@ -313,17 +314,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::CH16, 1024), C::IDESC_PV,
-                       (j > 1 || kk > 0) ? 1u : 0u);
+                mma_ts_w(tO, tS + kk * 8, v_lo + kk * (2048 >> 4), HI, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
               if (j == T.n[t]) mma_commit(BAR(E_OFULL + t));
             }
             if (j < T.n[t]) {
               // S_t = Q8_t K8_j^T: four K = 32 steps within the 128-byte swizzled rows
-              const uint32_t qbase = sbase + C::OFF_Q + t * C::T8;
+              const uint32_t q_lo = sdesc_sw128_lo(sbase + C::OFF_Q + t * C::T8, 16);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ss_f8(tS, sdesc_sw128(qbase + kk * 32, 16, 1024), sdesc_sw128(kbase + kk * 32, 16, 1024),
-                          C::IDESC_QK, kk > 0 ? 1u : 0u);
+                mma_ss_f8_w(tS, q_lo + kk * (32 >> 4), HI, k_lo + kk * (32 >> 4), HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
               mma_commit(BAR(E_SFULL + t));
             }
           }

@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int prev_n0 = 0, prev_n1 = 0, prev_nmax = 0;
       bool ok = true;
       const uint32_t qb = sbase + C::OFF_Q;
+      constexpr uint32_t HI = sdesc_sw128_hi(1024);
+      const uint32_t q0_lo = sdesc_sw128_lo(qb, 16), q1_lo = sdesc_sw128_lo(qb + C::TILE, 16);
       // PV_t of the block at ring position vpos: O_t (+)= P_t V; `last` marks the tile's
       // last block of its unit (its completion is what the epilogue waits for).
 #define PV_ISSUE(t, pvc, vpos, first, last)                                                              \
@@ -288,11 +290,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       ok = false;                                                                                         \
     } else {                                                                                              \
       tc_fence_after();                                                                                   \
-      const uint32_t vbase_ = sbase + C::OFF_RING + ((vpos) % C::NS) * C::TILE;                          \
+      const uint32_t vlo_ = sdesc_sw128_lo(sbase + C::OFF_RING + ((vpos) % C::NS) * C::TILE, C::CHUNK);   \
       const uint32_t tS_ = tmem + uint32_t((t) * 128), tO_ = tmem + 256u + uint32_t((t) * D);            \
       _Pragma("unroll") for (int kk = 0; kk < 8; ++kk)                                                    \
-        mma_ts(tO_, tS_ + kk * 8, sdesc_sw128(vbase_ + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,          \
-               (!(first) || kk > 0) ? 1u : 0u);                                                           \
+        mma_ts_w(tO_, tS_ + kk * 8, vlo_ + kk * (2048 >> 4), HI, C::IDESC_PV,                           \
+                 (!(first) || kk > 0) ? 1u : 0u);                                                         \
       ++(pvc);                                                                                            \
       if (last) mma_commit(BAR(P_OFULL + (t)));                                                           \
     }                                                                                                     \
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (!mbar_wait(BAR(P_FULL + kpos % C::NS), (kpos / C::NS) & 1, wc)) { ok = false; break; }
           if (G > 0 && !mbar_wait(BAR(P_FULL + vpos % C::NS), (vpos / C::NS) & 1, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kbase = sbase + C::OFF_RING + (kpos % C::NS) * C::TILE;
+          const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_RING + (kpos % C::NS) * C::TILE, 16);
           // Tile 0: PV of its previous block (if any), the unit's Q (before its first S;
           // tile 0 always has one at j = 0), S of block j.  Then the same for tile 1.
           do {
@@ -323,9 +325,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (j < T.n[0]) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                mma_ss(tmem, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
-                       kk > 0 ? 1u : 0u);
+                const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_w(tmem, q0_lo + off, HI, k_lo + off, HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
               }
               mma_commit(BAR(P_SFULL + 0));
             }
@@ -341,9 +342,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (j < T.n[1]) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                mma_ss(tmem + 128u, sdesc_sw128(qb + C::TILE + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                       C::IDESC_QK, kk > 0 ? 1u : 0u);
+                const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_w(tmem + 128u, q1_lo + off, HI, k_lo + off, HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
               }
               mma_commit(BAR(P_SFULL + 1));
             }

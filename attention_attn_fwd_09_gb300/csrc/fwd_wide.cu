@@ -287,18 +287,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       // of P_(j-1), which PV_(j-1) (issued earlier) has read: MMAs execute in issue order.
       bool ok = mbar_wait(BAR(V_Q), 0, wc);
       tc_fence_after();
-      const uint32_t qbase = sbase + C::OFF_Q;
+      // Matrix descriptors as low words advanced by (offset / 16), one constant high word.
+      constexpr uint32_t HI = sdesc_sw128_hi(1024);
+      const uint32_t q_lo = sdesc_sw128_lo(sbase + C::OFF_Q, 16);
       auto issue_s = [&](int j) -> bool {
         const int idx = pos_k(j), slot = idx % C::NS;
         if (!mbar_wait(BAR(V_FULL + slot), (idx / C::NS) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t kbase = sbase + C::OFF_RING + slot * C::TILE;
+        const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_RING + slot * C::TILE, 16);
         const uint32_t tS = tmem + uint32_t((j & 1) * 128);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::IDESC_QK,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss_w(tS, q_lo + off, HI, k_lo + off, HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
         mma_commit(BAR(V_SFULL + (j & 1)));
         return true;
@@ -320,14 +321,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t vbase = sbase + C::OFF_RING + vslot * C::TILE;
+        const uint32_t v_lo = sdesc_sw128_lo(sbase + C::OFF_RING + vslot * C::TILE, C::CHUNK);
         const uint32_t tS = tmem + uint32_t((j & 1) * 128), tO = tmem + 256u;
         // P of keys 16kk .. 16kk + 15: columns 8kk .. of the buffer; with SPLIT the second
         // half's keys sit at columns 64 .. 95 (each half writes inside its own scores).
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + (C::SPLIT && kk >= 4 ? 32 : 0) + kk * 8, sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024),
-                 C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tO, tS + (C::SPLIT && kk >= 4 ? 32 : 0) + kk * 8, v_lo + kk * (2048 >> 4), HI, C::IDESC_PV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(BAR(V_PVD + (j & 1)));
       }
       // Drain: every MMA issued above completes before TMEM is released.
