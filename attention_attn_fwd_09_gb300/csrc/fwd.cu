@@ -256,6 +256,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::NS; ++s) mbar_init(BAR(B_FULL + s), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // Thread 0 is also the producer: its first loads (the Q tiles, K_0 and V_0, which need no
+    // free slot) go out before the CTA-wide barrier, overlapping the TMEM allocation.
+    const uint32_t qtile = MODE == 1 ? p.q_tile_bytes : C::TILE;
+    mbar_arrive_expect_tx(BAR(B_Q), (T.n[0] > 0 ? qtile : 0) + (T.n[1] > 0 ? qtile : 0));
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (T.n[t] == 0) continue;
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(sbase + C::OFF_Q + t * C::TILE + c * C::CHUNK, &tm_q, c * 64, T.row0[t], T.bh[t], BAR(B_Q));
+    }
+    if (nmax > 0 && !p.test_skip_first_kv) {
+      for (int which = 0; which < 2; ++which) {
+        mbar_arrive_expect_tx(BAR(B_FULL + which), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sbase + C::OFF_RING + which * C::TILE + c * C::CHUNK, which ? &tm_v : &tm_k, c * 64,
+                      T.krow0 + T.j0 * 128, T.bkv, BAR(B_FULL + which));
+      }
+    }
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -277,25 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      const uint32_t qtile = MODE == 1 ? p.q_tile_bytes : C::TILE;
-      const uint32_t qbytes = (T.n[0] > 0 ? qtile : 0) + (T.n[1] > 0 ? qtile : 0);
-      mbar_arrive_expect_tx(BAR(B_Q), qbytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (T.n[t] == 0) continue;
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sbase + C::OFF_Q + t * C::TILE + c * C::CHUNK, &tm_q, c * 64, T.row0[t], T.bh[t], BAR(B_Q));
-      }
-      // next_idx: one past the last ring index handed to the TMA unit.  skip_idx: a ring
-      // index deliberately never loaded (test hook for the bounded-wait path), or -1.
+      // The Q tiles and ring indices 0 and 1 (K_0, V_0) were issued before the CTA-wide
+      // barrier.  next_idx: one past the last ring index handed to the TMA unit.  skip_idx: a
+      // ring index deliberately never loaded (test hook for the bounded-wait path: the first
+      // K and V are then both skipped), or -1.
       const int skip_idx = p.test_skip_first_kv ? 0 : -1;
-      int next_idx = 0;
+      int next_idx = nmax > 0 ? 2 : 0;
       bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
+      for (int j = 1; j < nmax && ok; ++j) {
         for (int which = 0; which < 2; ++which) {
           const int idx = 2 * j + which, slot = idx % C::NS;
           if (idx >= C::NS) {
@@ -320,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // only the last NS ring indices can be outstanding.
         const unsigned long long t0 = globaltimer_ns();
         for (int idx = max(0, next_idx - C::NS); idx < next_idx; ++idx) {
-          if (idx == skip_idx) continue;
+          if (skip_idx == 0 && idx < 2) continue;
           const uint32_t bar = BAR(B_FULL + idx % C::NS), par = (idx / C::NS) & 1;
           while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 < p.wait_ns) {
           }
@@ -598,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_commit();
       }
     }
-    if (warp == 12 && lane == 0) tma_store_wait_all();
+    if (warp == 12 && lane == 0) tma_store_wait_read();
   }
 
   tc_fence_before();

@@ -106,6 +106,11 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Wait until every committed bulk store has finished READING its shared-memory source (the
+// global writes complete on their own; they are visible once the kernel has finished).
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Order this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA / tensor core) reads of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
