@@ -494,9 +494,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // probabilities are computed while they run.  MMAs of one thread execute in issue
         // order: S^T lands in the columns of P^T only after dV has read them.
         if (it + 1 < n_iter && !issue_s(it + 1)) { ok = false; break; }
-        // dK += dS^T Q ; dQ^T = K^T dS^T
+        // dK += dS^T Q and dQ^T = K^T dS^T.  At d = 64 dQ^T goes first, so that the drain reads it
+        // while dK runs (the next dP^T waits for that read): measured 2.6 % faster there, and
+        // 9 % slower at d = 128, where the drain's reductions then overlap the compute warps'
+        // shared-memory traffic.
+        constexpr bool DQ_FIRST = D == 64;
         if (!mbar_wait(BAR(W_DS), it & 1, wc)) { ok = false; break; }
         tc_fence_after();
+        auto issue_dqt = [&]() {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            if constexpr (DET)
+              mma_ss(tdP, sdesc_sw128(sbase + C::OFF_K + kk * 2048, C::CHUNK, 1024),
+                     sdesc_sw128(sbase + C::OFF_DS + kk * 2048, C::CHUNK, 1024), C::IDESC_DQT, kk > 0);
+            else
+              mma_ss_w(tdP, kt_lo + kk * (2048 >> 4), HI, dst_lo + kk * (2048 >> 4), HI, C::IDESC_DQT, kk > 0);
+          mma_commit(BAR(W_DQ));
+        };
+        if constexpr (DQ_FIRST) issue_dqt();
         const uint32_t qt_lo = sdesc_sw128_lo(qs, C::CHUNK);   // Q, MN-major
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -508,15 +523,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_ss_w(tdK, ds_lo + off, HI, qt_lo + kk * (2048 >> 4), HI, C::IDESC_KB, (it > 0 || kk > 0));
         }
         mma_commit(BAR(W_EMPTY + st));  // dK was the stage's last reader: the producer may refill it
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          if constexpr (DET)
-            mma_ss(tdP, sdesc_sw128(sbase + C::OFF_K + kk * 2048, C::CHUNK, 1024),
-                   sdesc_sw128(sbase + C::OFF_DS + kk * 2048, C::CHUNK, 1024), C::IDESC_DQT, kk > 0);
-          else
-            mma_ss_w(tdP, kt_lo + kk * (2048 >> 4), HI, dst_lo + kk * (2048 >> 4), HI, C::IDESC_DQT, kk > 0);
-        mma_commit(BAR(W_DQ));
-        mma_commit(BAR(W_DSFREE));
+        if constexpr (!DQ_FIRST) issue_dqt();
+        mma_commit(BAR(W_DSFREE));      // dQ^T and dK, the readers of dS^T, are done
       }
       mma_commit(BAR(W_DONE));
       const unsigned long long t0 = globaltimer_ns();
