@@ -493,9 +493,10 @@ def rescale_lines(A, torch, dev):
 def _case_table():
     """Single-configuration runs for a profiler (``--case NAME``): name -> (description,
     setup(A, torch, dev) -> callable)."""
-    def fwd(b, h, hkv, n, d, causal, poly=0, recipe="normal", seed=3):
+    def fwd(b, h, hkv, n, d, causal, poly=0, recipe="normal", seed=3, persistent=False):
         def setup(A, torch, dev):
             from attn_inputs import make_inputs
+            A.attn_set_fwd_persistent(persistent)
             x = make_inputs(seed, b, h, hkv, n, d, recipe=recipe)
             q, k, v = (x[nm].to(dev) for nm in ("q", "k", "v"))
             o, lse = torch.empty_like(q), torch.empty((b, h, n), dtype=torch.float32, device=dev)
@@ -560,6 +561,12 @@ def _case_table():
         "fwd_d128_N8192_noncausal_poly4": ("same, 4 of 16 exponentials on the FMA cubic",
                                            fwd(2, 16, 16, 8192, 128, False, poly=4)),
         "fwd_d128_N4096_noncausal": ("forward B4 H16 N4096 d128 non-causal", fwd(4, 16, 16, 4096, 128, False)),
+        "fwd_d128_N2048_noncausal": ("forward B8 H16 N2048 d128 non-causal", fwd(8, 16, 16, 2048, 128, False)),
+        "fwd_d128_N2048_persistent": ("same, persistent kernel", fwd(8, 16, 16, 2048, 128, False, persistent=True)),
+        "fwd_d128_N4096_persistent": ("forward B4 H16 N4096 d128 non-causal, persistent kernel",
+                                      fwd(4, 16, 16, 4096, 128, False, persistent=True)),
+        "fwd_d128_N8192_persistent": ("forward B2 H16 N8192 d128 non-causal, persistent kernel",
+                                      fwd(2, 16, 16, 8192, 128, False, persistent=True)),
         "fwd_d64_N8192_noncausal": ("forward B2 H16 N8192 d64 non-causal", fwd(2, 16, 16, 8192, 64, False)),
         "fwd_d256_N8192_noncausal": ("forward B2 H16 N8192 d256 non-causal (one-tile kernel)",
                                      fwd(2, 16, 16, 8192, 256, False, seed=9)),
@@ -588,6 +595,8 @@ def _case_table():
         "bwd_d192_N8192_noncausal": ("backward B2 H16 N8192 d192 non-causal (column halves)",
                                      bwd(2, 16, 8192, 192, False)),
         "bwd_N8192_noncausal_det": ("same, deterministic dQ", bwd(2, 16, 8192, 128, False, det=True)),
+        "bwd_train_det": ("backward B4 H16 N2048 d128 non-causal, deterministic dQ",
+                          bwd(4, 16, 2048, 128, False, det=True, seed=2)),
         "varlen_fwd_noncausal": ("packed forward, 18 sequences (65536 tokens), H16 d128", varlen(False, False)),
         "varlen_bwd_noncausal": ("packed backward, same batch", varlen(True, False)),
         "fp8_fwd_N8192_noncausal": ("FP8 forward B2 H16 N8192 d128 non-causal", fwd_fp8(2, 8192, False)),
@@ -621,6 +630,7 @@ def run_case(args):
     torch.cuda.synchronize()
     A.attn_set_debug_knobs()
     A.attn_set_decode_one_tile(True)
+    A.attn_set_fwd_persistent(False)
     if A.attn_device_status(True) != 0:
         raise RuntimeError("a kernel reported a timeout")
     return {"case": args.case, "what": desc, "steps": args.steps, "warmup": args.warmup,
