@@ -35,7 +35,7 @@ NOMINAL_PEAK_TFLOPS = 2250.0
 WORKLOAD = dict(name="train_fwd_bwd_B4_H16_N2048_d128", seed=2, B=4, Hq=16, Hkv=16, N=2048, d=128, causal=False)
 FWD_SWEEP = (4096, 8192, 16384)          # forward-only lines at d=128, non-causal, B*N = 16384
 L2_FLUSH_BYTES = 512 << 20
-E2E_STREAMS = 4                           # end-to-end leg: batch chunks alternate over these streams
+E2E_STREAMS = 2                           # end-to-end leg: batch chunks' kernels alternate over these streams
 
 
 def fwd_flops(B, Hq, N, d, causal):
@@ -741,9 +741,11 @@ def run_ours(args):
     e2e_serial = combine(step_flops * K, world, serial_s) / 1e12
 
     # The same step pipelined the way a caller with host-resident data would run it: one
-    # chunk per batch element, alternating over E2E_STREAMS streams, so that one chunk's
-    # copies overlap another chunk's kernels.  Every chunk still copies its own inputs in
-    # and its results out inside the timed region.
+    # chunk per batch element; the input copies go in order on one copy stream, each chunk's
+    # kernels on one of two compute streams once its inputs have landed, and the result copies
+    # in order on a third stream, so that the two link directions and the kernels overlap.
+    # Every chunk still copies its own inputs in and its results out inside the timed region.
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
     ws_s = [torch.empty((max(A.attn_bwd_workspace_size(1, Hq, Hkv, N, d, False), 16),), dtype=torch.uint8,
                         device=dev) for _ in streams] if has_bwd else []
@@ -754,22 +756,30 @@ def run_ours(args):
     for i in range(K):
         flush.fill_(float(i))
         pe[i][0].record(main)
-        for st in streams:
+        for st in (s_in, s_out, *streams):
             st.wait_stream(main)
         for b in range(B):
-            si = b % len(streams)
-            with torch.cuda.stream(streams[si]):
-                sl = slice(b, b + 1)
+            sl = slice(b, b + 1)
+            cs = streams[b % len(streams)]
+            with torch.cuda.stream(s_in):
                 for t_d, t_h in zip((q, k, v, do) if has_bwd else (q, k, v), (q_h, k_h, v_h, do_h)):
                     t_d[sl].copy_(t_h[sl], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            cs.wait_event(ev_in)
+            with torch.cuda.stream(cs):
                 A.attn_fwd(q[sl], k[sl], v[sl], causal=causal, scale=scale, o=o[sl], lse=lse[sl])
                 if has_bwd:
                     A.attn_bwd(q[sl], k[sl], v[sl], o[sl], lse[sl], do[sl], causal=causal, scale=scale,
-                               dq=dq[sl], dk=dk[sl], dv=dv[sl], workspace=ws_s[si])
+                               dq=dq[sl], dk=dk[sl], dv=dv[sl], workspace=ws_s[b % len(streams)])
+                ev_c = torch.cuda.Event()
+                ev_c.record(cs)
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
                 for t_h, t_d in zip(outs_h, (o, dq, dk, dv)):
                     t_h[sl].copy_(t_d[sl], non_blocking=True)
                 lse_h[sl].copy_(lse[sl], non_blocking=True)
-        for st in streams:
+        for st in (s_in, s_out, *streams):
             main.wait_stream(st)
         pe[i][1].record(main)
     torch.cuda.synchronize()
@@ -778,6 +788,52 @@ def run_ours(args):
         raise RuntimeError("a kernel reported a timeout in the end-to-end leg")
     e2e_s = max_over_ranks(dist, sum(e[0].elapsed_time(e[1]) for e in pe) / 1e3, dev)
     e2e_value = combine(step_flops * K, world, e2e_s) / 1e12
+
+    # The host link itself: one pinned-to-device copy of the step's input bytes and one
+    # device-to-pinned copy of its output bytes, timed alone, as the ceiling of the leg above.
+    link = {}
+    for name, nbytes, to_dev in (("h2d", h2d, True), ("d2h", d2h, False)):
+        hb = torch.empty((nbytes,), dtype=torch.uint8, pin_memory=True)
+        db = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            (db.copy_(hb, non_blocking=True) if to_dev else hb.copy_(db, non_blocking=True))
+        le = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(5)]
+        for e in le:
+            e[0].record()
+            (db.copy_(hb, non_blocking=True) if to_dev else hb.copy_(db, non_blocking=True))
+            e[1].record()
+        torch.cuda.synchronize()
+        link[f"{name}_gbs"] = round(nbytes / statistics.median(e[0].elapsed_time(e[1]) for e in le) / 1e6, 1)
+        del hb, db
+    # Both directions at once (two streams), as the pipelined leg runs them.
+    hb_in = torch.empty((h2d,), dtype=torch.uint8, pin_memory=True)
+    db_in = torch.empty((h2d,), dtype=torch.uint8, device=dev)
+    hb_out = torch.empty((d2h,), dtype=torch.uint8, pin_memory=True)
+    db_out = torch.empty((d2h,), dtype=torch.uint8, device=dev)
+    sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    both = []
+    for r in range(8):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        sa.wait_stream(main)
+        sb.wait_stream(main)
+        with torch.cuda.stream(sa):
+            db_in.copy_(hb_in, non_blocking=True)
+        with torch.cuda.stream(sb):
+            hb_out.copy_(db_out, non_blocking=True)
+        main.wait_stream(sa)
+        main.wait_stream(sb)
+        e1.record(main)
+        torch.cuda.synchronize()
+        if r >= 3:
+            both.append(e0.elapsed_time(e1))
+    del hb_in, db_in, hb_out, db_out
+    # The slowest of the input copies, the result copies (or both at once) and the kernels
+    # bounds a step whose copies and kernels overlap perfectly: the end-to-end ceiling here.
+    h2d_ms, d2h_ms, both_ms = h2d / link["h2d_gbs"] / 1e6, d2h / link["d2h_gbs"] / 1e6, statistics.median(both)
+    link["h2d_ms"], link["d2h_ms"], link["both_directions_ms"] = round(h2d_ms, 4), round(d2h_ms, 4), round(both_ms, 4)
+    link["e2e_ceiling"] = round(step_flops / max(h2d_ms, d2h_ms, both_ms, statistics.mean(step_ms)) / 1e9, 1)
 
     # Forward-only lines at the lengths the forward target is stated for (d=128, non-causal).
     sweep = {}
@@ -840,8 +896,10 @@ def run_ours(args):
         "bwd_tflops": round(2.5 * ff / bwd_avg / 1e9, 1) if has_bwd else None,
         "frac_of_2250": round(value / world / NOMINAL_PEAK_TFLOPS, 4),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "pipelining": f"{B} batch chunks over {E2E_STREAMS} streams",
-                "serial_value": round(e2e_serial, 2)},
+                "d2h_bytes_per_step": d2h,
+                "pipelining": f"{B} batch chunks: inputs in order on one copy stream, kernels on {E2E_STREAMS} "
+                              "streams, results in order on another copy stream",
+                "serial_value": round(e2e_serial, 2), "host_link": link},
         "gpu_launches": K * (1 + (3 if has_bwd else 0)),
         "roofline": roofline,
         "clocks": clk.summary(),
