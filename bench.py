@@ -340,7 +340,8 @@ def _median_ms(torch, flush, call, reps=8, warm=3):
 
 
 def suite_lines(A, torch, dev, flush):
-    """The measurement suite's other configurations (forward sweep over N = 512 .. 16384,
+    """The measurement suite's other configurations (the training-shape step causal and not,
+    atomic and deterministic; the forward sweep over N = 512 .. 16384,
     d = 64 and 128, causal and not; grouped / multi-query heads at N = 8192 with outlier
     inputs; the backward at N = 8192 and 16384, atomic and deterministic).  Each line:
     median ms over 8 calls (L2 flushed before each), TFLOP/s, and the roofline ceiling
@@ -352,7 +353,25 @@ def suite_lines(A, torch, dev, flush):
     def fwd_bytes(B, Hq, Hkv, N, d):
         return 2.0 * (2 * B * Hq * N * d + 2 * B * Hkv * N * d) + 4.0 * B * Hq * N
 
-    res = {"sweep": {}, "gqa_outliers": {}, "bwd_long": {}}
+    res = {"sweep": {}, "gqa_outliers": {}, "bwd_long": {}, "train": {}}
+    # The training-shape step (B=4, H=16, N=2048, d=128, seed 2), causal and not, atomic and
+    # deterministic dQ: forward, backward and the step's TFLOP/s (3.5 x the forward FLOPs).
+    x = make_inputs(2, 4, 16, 16, 2048, 128, with_grad=True)
+    q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
+    o, lse = torch.empty_like(q), torch.empty((4, 16, 2048), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for causal in (False, True):
+        fl = fwd_flops(4, 16, 2048, 128, causal)
+        msf = _median_ms(torch, flush, lambda: A.attn_fwd(q, k, v, causal=causal, scale=128 ** -0.5, o=o, lse=lse))
+        for det in (False, True):
+            ws = torch.empty((A.attn_bwd_workspace_size(4, 16, 16, 2048, 128, det),), dtype=torch.uint8, device=dev)
+            msb = _median_ms(torch, flush, lambda: A.attn_bwd(q, k, v, o, lse, do, causal=causal, scale=128 ** -0.5,
+                                                              deterministic=det, dq=dq, dk=dk, dv=dv, workspace=ws))
+            res["train"][f"{'causal' if causal else 'noncausal'}_{'det' if det else 'atomic'}"] = {
+                "fwd_ms": round(msf, 4), "bwd_ms": round(msb, 4), "fwd_tflops": round(fl / msf / 1e9, 1),
+                "bwd_tflops": round(2.5 * fl / msb / 1e9, 1), "step_tflops": round(3.5 * fl / (msf + msb) / 1e9, 1)}
+            del ws
+    del x, q, k, v, do, o, lse, dq, dk, dv
     for d in (64, 128):
         for n in (512, 1024, 2048, 4096, 8192, 16384):
             b = 16384 // n

@@ -60,8 +60,9 @@ def test_shapes(A, d, shape, causal, deterministic):
 
 @pytest.mark.parametrize("d", [192, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_long_sampled_heads(A, d, causal):
-    B, H, N = 2, 8, 4096
+@pytest.mark.parametrize("N", [4096, 8192])
+def test_long_sampled_heads(A, d, causal, N):
+    B, H = 8192 // N, 8
     x = make_inputs(5, B, H, H, N, d, with_grad=True)
     scale = default_scale(d)
     dq, dk, dv = run_bwd(A, x, causal, scale)
