@@ -36,12 +36,19 @@ namespace attn {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Deterministic mode splits a tile's contributions into up to this many classes, each with
+// its own counter and accumulator (see the kernel).
+constexpr int kDetMaxClasses = 2;
+
+// Layout: dQacc [B, Hq, ceil(N/128)*128, d] fp32, delta and LSE2 [B, Hq, N] fp32, and when
+// deterministic the counters [kDetMaxClasses][B, Hq, ceil(N/128)] and kDetMaxClasses - 1
+// more accumulators shaped as dQacc, each starting on a 256-byte boundary.
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic) {
   (void)Hkv;
   const size_t rows = (size_t)B * Hq * N;
   const size_t nq = (size_t)B * Hq * ((N + 127) / 128);
   size_t n = align256(nq * 128 * d * 4) + 2 * align256(rows * 4);
-  if (deterministic) n += align256(nq * 4);
+  if (deterministic) n += align256(kDetMaxClasses * nq * 4) + (kDetMaxClasses - 1) * align256(nq * 128 * d * 4);
   return n;
 }
 
@@ -80,6 +87,8 @@ void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int det
   p->lse2 = reinterpret_cast<float*>(b);
   b += align256(rows * 4);
   p->sem = deterministic ? reinterpret_cast<int*>(b) : nullptr;
+  b += deterministic ? align256(kDetMaxClasses * nq * 4) : 0;
+  p->dq_acc2 = deterministic ? reinterpret_cast<float*>(b) : nullptr;
 }
 
 namespace {
@@ -106,6 +115,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
                                                               const uint16_t* __restrict__ dout,
                                                               const float* __restrict__ lse, float* __restrict__ delta,
                                                               float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                              float* __restrict__ dq_extra, int n_extra,
+                                                              long long extra_stride,
                                                               int* __restrict__ sem, long long rows, int N, int npad,
                                                               int n_sem, const int* __restrict__ cu_q, int nseq,
                                                               long long rows_pad) {
@@ -145,6 +156,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
   float4* z = reinterpret_cast<float4*>(dq_acc + zrow * D + sub * PER);
 #pragma unroll
   for (int i = 0; i < PER / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int x = 0; x < n_extra; ++x) {
+    float4* z2 = reinterpret_cast<float4*>(dq_extra + x * extra_stride + zrow * D + sub * PER);
+#pragma unroll
+    for (int i = 0; i < PER / 4; ++i) z2[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (sub == 0) {
     delta[row] = acc;
     lse2[row] = lse[row] * kLog2e;
@@ -152,18 +168,29 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 }
 
 // ------------------------------------------------------------------------------------
-// Convert: dq = bf16(scale * dQacc), 8 elements per thread (dQacc rows padded per head).
+// Convert: dq = bf16(scale * dQacc), 8 elements per thread (dQacc rows padded per head);
+// with more accumulators, dq = bf16(scale * (((dQacc + dQacc_1) + dQacc_2) + ...)), always in
+// that order.
 // ------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ acc,
+                                                           const float* __restrict__ extra, int n_extra,
+                                                           long long extra_stride, uint16_t* __restrict__ dq,
                                                            float scale, long long n8, int N, int npad,
                                                            const int* __restrict__ cu_q, int nseq, long long rows_pad) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / (D / 8), bh = row / N, rr = row - bh * N;
     const long long arow = cu_q ? bh * rows_pad + rr + 128LL * seq_of(cu_q, nseq, (int)rr) : bh * npad + rr;
     const long long src = (arow * D) / 8 + i % (D / 8);
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * src];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * src + 1];
+    float4 a = reinterpret_cast<const float4*>(acc)[2 * src];
+    float4 b = reinterpret_cast<const float4*>(acc)[2 * src + 1];
+    for (int x = 0; x < n_extra; ++x) {
+      const float4* acc2 = reinterpret_cast<const float4*>(extra + x * extra_stride);
+      const float4 a2 = acc2[2 * src];
+      const float4 b2 = acc2[2 * src + 1];
+      a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
+      b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
+    }
     uint4 r;
     r.x = pack_bf16x2(a.x * scale, a.y * scale);
     r.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -209,7 +236,9 @@ enum {
   W_VFULL = 14,   // -LSE2 and -D of the next tile are in shared memory (32 arrivals, warp 3)
   W_GD = 15,
   W_VFREE = 16,   // both compute warpgroups are done with those vectors (256 arrivals)
-  W_COUNT = 17
+  W_ADDED = 17,   // deterministic: the drain has issued a tile's additions (128 arrivals)
+  W_RELEASED = 18,  // deterministic: the releaser has passed that tile's counter on (1)
+  W_COUNT = 19
 };
 
 // Bounded barrier for one warpgroup (128 threads) built on an mbarrier: every thread
@@ -265,10 +294,14 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 struct BwdKernelArgs {
   int B, Hq, Hkv, N, g, nq, nkb, causal, deterministic;
   int det_rotate;   // deterministic with the rotating per-tile order (see the kernel)
+  int det_k;        // deterministic: contribution classes (1 or 2), one accumulator each
+  int det_releaser; // deterministic: warp 2 passes the counters on (else the drain leader)
   float c, scale;
   const float* lse2;
   const float* delta;
   float* dq_acc;
+  float* dq_extra;  // deterministic: accumulators 1 .. det_k - 1, extra_stride floats apart
+  long long extra_stride;
   int* sem;
   unsigned long long wait_ns;
   int* status;
@@ -346,7 +379,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_COUNT; ++i)
       mbar_init(BAR(i), (i == W_P || i == W_DS || i == W_VFREE) ? 256
-                        : (i == W_DQFREE || i == W_EPI || i == W_GD) ? 128 : (i == W_VFULL) ? 32 : 1);
+                        : (i == W_DQFREE || i == W_EPI || i == W_GD || i == W_ADDED) ? 128
+                        : (i == W_VFULL) ? 32 : 1);
     // W_EMPTY: released by a commit once the stage's last MMA (dK) has finished.
     *abort_flag = 0;
     fence_mbar_init();
@@ -384,6 +418,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     m = m_start + m_step * (it - r * n_m);
     if (m >= nqt) m -= nqt;                          // non-causal rotation wraps around
     bh = (VL ? 0 : b * a.Hq) + hkv * a.g + r;
+  };
+  // Deterministic: iteration it's counter, accumulator and turn.  A block's place among a
+  // tile's contributions (its iteration with the rotating order, its index with the shared
+  // one) splits them into det_k classes, place mod det_k, each added into its own
+  // accumulator in its own order (the convert kernel sums the accumulators in a fixed
+  // order).  A block then waits for the contribution det_k places before its own instead
+  // of the one just before: with the rotating order det_k iterations of slack, with the
+  // shared order a chain det_k times shorter, so the round trip of one addition (poll,
+  // adds, fence, counter) sets the pace less.  Packed sequences: one class; the counters
+  // of a sequence's tiles start at (q0 + 128 b) / 128.
+  auto det_slot = [&](int it, int*& sem, float*& acc, int& turn) {
+    int bh, m;
+    iter_head_row(it, bh, m);
+    const int place = a.det_rotate ? it - (it / n_m) * n_m : n;
+    const int cls = place & (a.det_k - 1);
+    turn = place / a.det_k;
+    acc = cls ? a.dq_extra + (size_t)(cls - 1) * a.extra_stride : a.dq_acc;
+    if constexpr (VL) sem = a.sem + (size_t)bh * a.sem_stride + (q0 + 128 * b) / 128 + m;
+    else sem = a.sem + (size_t)cls * a.B * a.Hq * a.nq + (size_t)bh * a.nq + m;
   };
 
   // Register split (per thread): warpgroup 0 (producer, MMA) 88, the two compute
@@ -560,6 +613,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(BAR(W_VFULL));
       if (it + 1 < n_iter) fetch(it + 1);
     }
+  } else if (DET && warp == 2) {
+    // ------------------------------------------------------------------ releaser
+    // Passes each tile's counter on once the drain has issued the tile's additions: the
+    // drain's arrivals (release, CTA scope) order its additions before this thread's
+    // gpu-scope fence, which is cumulative, and that fence before the increment.  The
+    // fence waits for the additions to land; here it delays no TMEM read of the drain.
+    if (a.det_releaser && lane == 0) {
+      for (int it = 0; it < n_iter; ++it) {
+        if (!mbar_wait(BAR(W_ADDED), it & 1, wc) || *abort_flag) break;
+        int* sem;
+        float* acc;
+        int turn;
+        det_slot(it, sem, acc, turn);
+        __threadfence();
+        atomicAdd(sem, 1);
+        mbar_arrive(BAR(W_RELEASED));
+      }
+    }
+    __syncwarp();
   }
   } else if (wg == 1 || wg == 2) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;");
@@ -747,12 +819,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Rows are padded to whole tiles, so queries past N (or past the sequence) add into
     // padding rows, which are never read.  Packed sequences: a sequence's rows start at
     // q0 + 128 b of its head's rows.
-    auto add_dq = [&](int bh, int m, const float (&v)[128]) {
+    auto add_dq = [&](float* acc, int bh, int m, const float (&v)[128]) {
       if (!has_col) return;
       size_t arow;
       if constexpr (VL) arow = (size_t)bh * a.rows_pad + q0 + 128 * (size_t)b + (size_t)m * 128;
       else arow = (size_t)bh * a.nq * 128 + (size_t)m * 128;
-      red_add_rows<D>(a.dq_acc + arow * D + dcol, v, std::make_integer_sequence<int, 8>{});
+      red_add_rows<D>(acc + arow * D + dcol, v, std::make_integer_sequence<int, 8>{});
     };
     if constexpr (!DET) {
       for (int it = 0; it < n_iter; ++it) {
@@ -760,21 +832,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         iter_head_row(it, bh, m);
         float v[128];
         if (!read_dq(it, v)) break;
-        add_dq(bh, m, v);
+        add_dq(a.dq_acc, bh, m, v);
       }
     } else {
       int gphase = 0;
       for (int it = 0; it < n_iter; ++it) {
         int bh, m;
         iter_head_row(it, bh, m);
-        // Packed sequences: the counters of a sequence's tiles start at (q0 + 128 b) / 128.
         int* sem;
-        if constexpr (VL) sem = a.sem + (size_t)bh * a.sem_stride + (q0 + 128 * b) / 128 + m;
-        else sem = a.sem + (size_t)bh * a.nq + m;
-        // This block's turn among the tile's contributions (see the tile order above).  The
-        // leader waits for it before the tile's dQ is ready, so the poll's round trip stays
-        // off the critical path (a turn depends only on other blocks' earlier additions).
-        const int turn = a.det_rotate ? it - (it / n_m) * n_m : n;
+        float* acc;
+        int turn;
+        det_slot(it, sem, acc, turn);
+        // The leader waits for the turn before the tile's dQ is ready, so the poll's round
+        // trip stays off the critical path (a turn depends only on other blocks' earlier
+        // additions).
         if (leader) {
           const unsigned long long t0 = globaltimer_ns();
           while (ld_acquire(sem) != turn) {
@@ -791,14 +862,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // Every drain thread learns that the turn has come (the leader's acquire, passed on
         // through the group barrier).
         if (!group_sync(BAR(W_GD), gphase, wc) || *abort_flag) break;
-        add_dq(bh, m, v);
-        // Release: the group barrier (its arrival releases at CTA scope) orders every
-        // drain thread's additions before the leader's gpu-scope fence, which is
-        // cumulative, and that fence before the counter's increment.
-        if (!group_sync(BAR(W_GD), gphase, wc)) break;
-        if (leader) {
-          __threadfence();
-          atomicAdd(sem, 1);
+        add_dq(acc, bh, m, v);
+        if (a.det_releaser) {
+          // Hand the tile to the releaser (warp 2), at most one tile ahead of it.
+          if (it > 0 && !warp_wait_b(BAR(W_RELEASED), (it - 1) & 1, wc)) break;
+          mbar_arrive(BAR(W_ADDED));
+        } else {
+          // Release here: the group barrier (its arrival releases at CTA scope) orders
+          // every drain thread's additions before the leader's gpu-scope fence, which is
+          // cumulative, and that fence before the counter's increment.
+          if (!group_sync(BAR(W_GD), gphase, wc)) break;
+          if (leader) {
+            __threadfence();
+            atomicAdd(sem, 1);
+          }
         }
       }
     }
@@ -819,23 +896,36 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   // Packed sequences: N is total_q and B the number of sequences, so a head has N rows.
   const long long rows = VL ? (long long)p.Hq * p.N : (long long)p.B * p.Hq * p.N;
   const int nq = (p.N + 127) / 128;
-  const int n_sem = !p.deterministic ? 0 : VL ? p.Hq * p.sem_stride : p.B * p.Hq * nq;
+  const int n_sem = !p.deterministic ? 0 : VL ? p.Hq * p.sem_stride : kDetMaxClasses * p.B * p.Hq * nq;
   const long long rows_pad = VL ? (long long)p.N + 128LL * p.B : 0;
   const int* cu_q = VL ? p.cu_q : nullptr;
+  int dev = 0, sms = 152;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // The rotating deterministic order (see the kernel) needs every key block of a head on
+  // the GPU at once: enabled when a head's blocks take at most half the SMs.
+  const bool rotate = !VL && DET && !p.causal && 2 * nq <= sms;
+  // Deterministic, measured on GB300 (B2 H16 d128): two classes cut the non-causal cost
+  // (N = 8192, rotating: 3.60 -> 3.27 ms; N = 16384, shared: 6.77 -> 6.00 ms, both with the
+  // releaser; four classes gained at most 6 % more and lost 5 % at N = 2048) but not the
+  // causal one, whose second accumulator only costs its zeroing and reading; the releaser
+  // helps wherever it is used here (causal N = 8192: 1.71 -> 1.49 ms) but, with one class,
+  // not the non-causal shared order (N = 16384: 6.77 -> 7.47 ms).
+  const int det_k = DET && !VL && !p.causal ? 2 : 1;
+  const int det_rel = DET && (det_k > 1 || p.causal) ? 1 : 0;
+  float* const extra = det_k > 1 ? p.dq_acc2 : nullptr;
+  const long long extra_stride = (long long)(align256((size_t)p.B * p.Hq * nq * 128 * D * 4) / 4);
   {
     const long long blocks = std::max((rows + 15) / 16, ((long long)n_sem + 255) / 256);
     if (blocks > 0) {
       bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
           static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.delta, p.lse2, p.dq_acc,
-          p.sem, rows, p.N, nq * 128, n_sem, cu_q, p.B, rows_pad);
-      cudaError_t e = cudaGetLastError();
+          extra, det_k - 1, extra_stride, p.sem, rows, p.N, nq * 128, n_sem, cu_q, p.B, rows_pad);
+      e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
   }
-  int dev = 0, sms = 152;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   {
     auto kern = attn_bwd_kernel<D, VL, DET>;
     constexpr uint32_t smem = BwdCfg<D>::SMEM;
@@ -848,9 +938,12 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     std::conditional_t<VL, BwdKernelArgsVL, BwdKernelArgs> a{};
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.N = p.N; a.g = p.g; a.nq = nq; a.nkb = nq;
     a.causal = p.causal; a.deterministic = p.deterministic;
-    a.det_rotate = (!VL && p.deterministic && !p.causal && 2 * nq <= sms) ? 1 : 0;
+    a.det_rotate = rotate ? 1 : 0;
+    a.det_k = det_k;
+    a.det_releaser = det_rel;
     a.c = p.c; a.scale = p.scale;
-    a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
+    a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.dq_extra = extra; a.extra_stride = extra_stride;
+    a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
     long long grid = (long long)p.B * p.Hkv * nq;
     if constexpr (VL) {
@@ -870,8 +963,9 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
     const long long n8 = rows * D / 8;
     const long long blocks = std::min<long long>((n8 + 255) / 256, (long long)sms * 8);
     if (blocks > 0) {
-      bwd_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, static_cast<uint16_t*>(p.dq), p.scale, n8,
-                                                              p.N, nq * 128, cu_q, p.B, rows_pad);
+      bwd_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(p.dq_acc, extra, det_k - 1, extra_stride,
+                                                              static_cast<uint16_t*>(p.dq), p.scale, n8, p.N,
+                                                              nq * 128, cu_q, p.B, rows_pad);
     }
     return cudaGetLastError();
   }

@@ -116,6 +116,8 @@ struct BwdParams {
   float* delta;              // [B, Hq, N] fp32 workspace (rowsum(dO o O))
   float* lse2;               // [B, Hq, N] fp32 workspace (LSE * log2 e)
   int* sem;                  // deterministic-order counters
+  float* dq_acc2;            // deterministic, d <= 128, not packed: the second accumulator
+                             // (shaped as dq_acc); null otherwise
   unsigned long long wait_ns;
   int* status;
   // Packed sequences (varlen = 1): N is total_q, Q/O/dO/dQ [Hq, total_q, D], K/V/dK/dV
@@ -139,7 +141,8 @@ struct BwdVarlenLayout {
   int sem_stride;
 };
 BwdVarlenLayout bwd_varlen_layout(int B, int Hq, int Hkv, int total_q, int total_k, int d, int deterministic);
-// Points p->dq_acc, delta, lse2, sem into the caller's workspace.
+// Points p->dq_acc, delta, lse2, sem (and, deterministic, dq_acc2) into the caller's
+// workspace.
 void bwd_workspace_carve(void* ws, int B, int Hq, int Hkv, int N, int d, int deterministic, BwdParams* p);
 // Backward for d = 192, 256 (bwd_wide.cu): maps as launch_bwd except q and dout, whose
 // boxes are 64 rows; workspace: dQacc [B, Hq, ceil(N/64)*64, d], D and LSE2 [B, Hq, N],
