@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
     T = map_unit_varlen(p, p.vl_units[blockIdx.x]);
   } else if constexpr (MODE == 1) {
+    // The merge kernel that follows is launched as a programmatic dependent: let it start
+    // (it waits for this grid's completion before reading the partial results).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     T = map_unit_grouped(p, blockIdx.x);
   } else if ((int)blockIdx.x < p.split_from) {
     T = map_unit(p, blockIdx.x);
@@ -668,6 +671,9 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int D, int poly,
 template <int D>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdParams p, uint16_t* __restrict__ o) {
   constexpr int PER = D / 32;
+  // Launched as a programmatic dependent of the split kernel: wait until that grid has
+  // completed and its partial results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gN = p.g * p.N, units = p.B * p.Hkv;
   const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wid >= (long long)units * gN) return;
@@ -708,10 +714,24 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdParams p, uint1
 cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t s) {
   const long long warps = (long long)p.B * p.Hkv * p.g * p.N;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
-  if (D == 64) fwd_merge_kernel<64><<<blocks, 256, 0, s>>>(p, static_cast<uint16_t*>(o));
-  else if (D == 128) fwd_merge_kernel<128><<<blocks, 256, 0, s>>>(p, static_cast<uint16_t*>(o));
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (blocks == 0) return cudaSuccess;
+  // Programmatic dependent launch: the merge's blocks are scheduled while the split kernel
+  // still runs (on SMs it leaves free) and wait in griddepcontrol.wait for its completion,
+  // instead of being launched after it.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t* op = static_cast<uint16_t*>(o);
+  if (D == 64) return cudaLaunchKernelEx(&cfg, fwd_merge_kernel<64>, p, op);
+  if (D == 128) return cudaLaunchKernelEx(&cfg, fwd_merge_kernel<128>, p, op);
+  return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------------------------------

@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
     T = map_wide_varlen(p, p.vl_units[blockIdx.x]);
   } else if constexpr (GRP) {
+    // The merge kernel that follows is launched as a programmatic dependent: let it start
+    // (it waits for this grid's completion before reading the partial results).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     T = map_wide_grouped(p, blockIdx.x);
   } else {
     T = map_wide(p, blockIdx.x);
