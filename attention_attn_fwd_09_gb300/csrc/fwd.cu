@@ -214,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int wg = warp >> 2;
+  // A kernel launched after this one as a programmatic dependent (the decode merge, the
+  // backward's preprocess) may be scheduled now; it waits for this grid's completion before
+  // reading what it writes.
+  pdl_trigger();
   // CTAs past split_from each take one tile of a unit (the other half of the unit goes to
   // the next CTA); the lone tile always sits in slot 0.
   Tiles T;
@@ -223,9 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
     T = map_unit_varlen(p, p.vl_units[blockIdx.x]);
   } else if constexpr (MODE == 1) {
-    // The merge kernel that follows is launched as a programmatic dependent: let it start
-    // (it waits for this grid's completion before reading the partial results).
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     T = map_unit_grouped(p, blockIdx.x);
   } else if ((int)blockIdx.x < p.split_from) {
     T = map_unit(p, blockIdx.x);
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdParams p, uint1
   constexpr int PER = D / 32;
   // Launched as a programmatic dependent of the split kernel: wait until that grid has
   // completed and its partial results are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
   const int gN = p.g * p.N, units = p.B * p.Hkv;
   const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wid >= (long long)units * gN) return;
@@ -716,21 +717,11 @@ cudaError_t launch_fwd_merge(const FwdParams& p, int D, void* o, cudaStream_t s)
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (blocks == 0) return cudaSuccess;
   // Programmatic dependent launch: the merge's blocks are scheduled while the split kernel
-  // still runs (on SMs it leaves free) and wait in griddepcontrol.wait for its completion,
-  // instead of being launched after it.
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // still runs (on SMs it leaves free) and wait in pdl_wait for its completion, instead of
+  // being launched after it.
   uint16_t* op = static_cast<uint16_t*>(o);
-  if (D == 64) return cudaLaunchKernelEx(&cfg, fwd_merge_kernel<64>, p, op);
-  if (D == 128) return cudaLaunchKernelEx(&cfg, fwd_merge_kernel<128>, p, op);
+  if (D == 64) return launch_pdl(fwd_merge_kernel<64>, dim3(blocks), dim3(256), 0, s, p, op);
+  if (D == 128) return launch_pdl(fwd_merge_kernel<128>, dim3(blocks), dim3(256), 0, s, p, op);
   return cudaErrorInvalidValue;
 }
 

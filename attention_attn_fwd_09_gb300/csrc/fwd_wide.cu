@@ -193,6 +193,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int wg = warp >> 2;
+  // A kernel launched after this one as a programmatic dependent (the decode merge, the
+  // backward's preprocess) may be scheduled now; it waits for this grid's completion before
+  // reading what it writes.
+  pdl_trigger();
   WideTile T;
   if constexpr (VL) {
     // CTAs past the table's records have no work: they leave before touching barriers or
@@ -200,9 +204,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if ((int)blockIdx.x >= __ldg(p.vl_count)) return;
     T = map_wide_varlen(p, p.vl_units[blockIdx.x]);
   } else if constexpr (GRP) {
-    // The merge kernel that follows is launched as a programmatic dependent: let it start
-    // (it waits for this grid's completion before reading the partial results).
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     T = map_wide_grouped(p, blockIdx.x);
   } else {
     T = map_wide(p, blockIdx.x);

@@ -108,6 +108,13 @@ __device__ __forceinline__ void tma_store_wait_all() {
 }
 // Wait until every committed bulk store has finished READING its shared-memory source (the
 // global writes complete on their own; they are visible once the kernel has finished).
+// Programmatic dependent launch.  pdl_trigger: this CTA lets the next grid of the stream
+// (if launched with programmatic stream serialization) be scheduled.  pdl_wait: the calling
+// thread waits until the grids this one depends on have completed and their writes are
+// visible (a no-op without such a dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
