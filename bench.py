@@ -576,6 +576,8 @@ def _case_table():
         return setup
 
     return {
+        "fwd_train_B4_H16_N2048": ("forward B4 H16 N2048 d128 non-causal (the training step's inputs)",
+                                   fwd(4, 16, 16, 2048, 128, False, seed=2)),
         "fwd_d128_N8192_noncausal": ("forward B2 H16 N8192 d128 non-causal", fwd(2, 16, 16, 8192, 128, False)),
         "fwd_d128_N8192_noncausal_poly4": ("same, 4 of 16 exponentials on the FMA cubic",
                                            fwd(2, 16, 16, 8192, 128, False, poly=4)),
