@@ -122,6 +122,64 @@ def test_deterministic_bit_identical(A, causal):
     assert len(digests) == 1
 
 
+@pytest.mark.parametrize("shape", [(1, 4, 4, 16384), (1, 8, 2, 4096)], ids=["shared_order_N16384", "gqa_N4096"])
+def test_deterministic_other_orders(A, shape):
+    # Non-causal at N = 16384 (128 key blocks per head, more than half the SMs): one shared
+    # tile order per head, contributions split into two classes.  Grouped heads at N = 4096:
+    # the rotating order walks each of a K/V head's query heads in turn.  Both repeat bit for
+    # bit and agree with the atomic order.
+    B, Hq, Hkv, N = shape
+    d = 128
+    x = make_inputs(77 + N, B, Hq, Hkv, N, d, with_grad=True)
+    scale = default_scale(d)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = A.attn_fwd(q, k, v, causal=False, scale=scale)
+    ws = torch.empty(A.attn_bwd_workspace_size(B, Hq, Hkv, N, d, True), dtype=torch.uint8, device=dev)
+    digests = set()
+    for _ in range(3):
+        ws.fill_(0x5A)
+        grads = A.attn_bwd(q, k, v, o, lse, do, causal=False, scale=scale, deterministic=True, workspace=ws)
+        torch.cuda.synchronize()
+        digests.add(_digest(grads))
+    atomic = A.attn_bwd(q, k, v, o, lse, do, causal=False, scale=scale, deterministic=False)
+    torch.cuda.synchronize()
+    assert A.attn_device_status(True) == 0
+    assert len(digests) == 1
+    for g, a in zip(grads, atomic):
+        assert rel_fro(g.float().cpu().numpy(), a.float().cpu().numpy()) <= GRAD_REL_FRO
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_inputs_written_just_before(A, deterministic):
+    # The backward's kernels are launched as programmatic dependents, and the main kernel
+    # starts loading Q, K, V and dO before it waits on the kernel before it: inputs written by
+    # the stream's previous kernels, with no synchronisation in between, must still be seen.
+    B, H, N, d = 2, 4, 1024, 128
+    x = make_inputs(88, B, H, H, N, d, with_grad=True)
+    scale = default_scale(d)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = A.attn_fwd(q, k, v, causal=False, scale=scale)
+    ref = [t.clone() for t in A.attn_bwd(q, k, v, o, lse, do, causal=False, scale=scale, deterministic=True)]
+    saved = [t.clone() for t in (q, k, v, do)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for t in (q, k, v, do):
+            t.zero_()
+        torch.cuda.synchronize()
+        for t, src in zip((q, k, v, do), saved):
+            t.copy_(src)                       # kernels immediately ahead of the backward
+        got = A.attn_bwd(q, k, v, o, lse, do, causal=False, scale=scale, deterministic=deterministic)
+        torch.cuda.synchronize()
+        if deterministic:
+            assert all(torch.equal(g, r) for g, r in zip(got, ref))
+        else:
+            for g, r in zip(got, ref):
+                assert rel_fro(g.float().cpu().numpy(), r.float().cpu().numpy()) <= 1e-3
+    assert A.attn_device_status(True) == 0
+
+
 def test_grouped_long(A):
     # GQA group of 4 sharing each K/V head; dK/dV sum over the group inside one CTA.
     w = WORKLOADS["gqa8k"]
