@@ -19,7 +19,7 @@ consecutive rows of one head, the tile the kernels load):
   forward    the attention definition (oracle/attn_oracle.c) applied to the dequantised
              Q~, K~, V~ in fp64: O = softmax(scale Q~ K~^T [causal]) V~, LSE by rows.
 
-So the FP8 path is judged against the exact attention of the values it was actually given;
+So the FP8 path is compared against the exact attention of the values it was actually given;
 the quantisation error itself is a property of the inputs, not of the kernel.
 """
 from __future__ import annotations
