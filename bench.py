@@ -626,6 +626,8 @@ def _case_table():
         "bwd_N16384_noncausal_det": ("backward B1 H16 N16384 d128 non-causal, deterministic dQ",
                                      bwd(1, 16, 16384, 128, False, det=True)),
         "bwd_N16384_noncausal": ("backward B1 H16 N16384 d128 non-causal", bwd(1, 16, 16384, 128, False)),
+        "bwd_N16384_causal_det": ("backward B1 H16 N16384 d128 causal, deterministic dQ",
+                                  bwd(1, 16, 16384, 128, True, det=True)),
         "varlen_fwd_noncausal": ("packed forward, 18 sequences (65536 tokens), H16 d128", varlen(False, False)),
         "varlen_bwd_noncausal": ("packed backward, same batch", varlen(True, False)),
         "fp8_fwd_N8192_noncausal": ("FP8 forward B2 H16 N8192 d128 non-causal", fwd_fp8(2, 8192, False)),
