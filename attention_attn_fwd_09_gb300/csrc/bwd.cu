@@ -108,7 +108,9 @@ __device__ __forceinline__ int seq_of(const int* __restrict__ cu, int B, int r) 
 }
 
 // ------------------------------------------------------------------------------------
-// Preprocess: one 16-thread group per row (d = 128: 8 bf16 per thread; d = 64: 4).
+// Preprocess: one 16-thread group per row (d = 128: 8 bf16 per thread; d = 64: 4); the
+// grid's y index walks the heads (bh), x the head's rows in groups of 16, so that no
+// thread divides by N.
 // ------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __restrict__ o,
@@ -125,17 +127,24 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
   // kernel's writes (O, LSE, dO), then let the main kernel be scheduled.
   pdl_wait();
   pdl_trigger();
-  const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
+  const long long nthreads = (long long)gridDim.x * gridDim.y * blockDim.x;
+  for (long long g = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; g < n_sem;
+       g += nthreads)
+    sem[g] = 0;
+  // Rows past N (the last group of a head) take part in the shuffles below with zeros and
+  // store nothing.
+  const int r = blockIdx.x * 16 + (threadIdx.x >> 4);   // row within the head
+  const bool valid = r < N;
   const int sub = threadIdx.x & 15;
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (sem != nullptr && gtid < n_sem) sem[gtid] = 0;
-  if (row >= rows) return;
+  const long long n_heads = rows / N;
+  for (long long bh = blockIdx.y; bh < n_heads; bh += gridDim.y) {
+  const long long row = bh * N + (valid ? r : 0);
   const uint16_t* orow = o + row * D + sub * PER;
   const uint16_t* drow = dout + row * D + sub * PER;
   float acc = 0.f;
   if constexpr (PER == 8) {
-    const uint4 a = *reinterpret_cast<const uint4*>(orow);
-    const uint4 b = *reinterpret_cast<const uint4*>(drow);
+    const uint4 a = valid ? *reinterpret_cast<const uint4*>(orow) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 b = valid ? *reinterpret_cast<const uint4*>(drow) : make_uint4(0u, 0u, 0u, 0u);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -143,8 +152,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
       acc = fmaf(__uint_as_float(av[i] & 0xffff0000u), __uint_as_float(bv[i] & 0xffff0000u), acc);
     }
   } else {
-    const uint2 a = *reinterpret_cast<const uint2*>(orow);
-    const uint2 b = *reinterpret_cast<const uint2*>(drow);
+    const uint2 a = valid ? *reinterpret_cast<const uint2*>(orow) : make_uint2(0u, 0u);
+    const uint2 b = valid ? *reinterpret_cast<const uint2*>(drow) : make_uint2(0u, 0u);
     const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -154,9 +163,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
-  const long long bh = row / N, r = row - bh * N;
+  if (!valid) continue;
   // Packed sequences (cu_q set): row r of sequence b sits at r + 128 b of its head's rows.
-  const long long zrow = cu_q ? bh * rows_pad + r + 128LL * seq_of(cu_q, nseq, (int)r) : bh * npad + r;
+  const long long zrow = cu_q ? bh * rows_pad + r + 128LL * seq_of(cu_q, nseq, r) : bh * npad + r;
   float4* z = reinterpret_cast<float4*>(dq_acc + zrow * D + sub * PER);
 #pragma unroll
   for (int i = 0; i < PER / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -169,12 +178,13 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
     delta[row] = acc;
     lse2[row] = lse[row] * kLog2e;
   }
+  }
 }
 
 // ------------------------------------------------------------------------------------
 // Convert: dq = bf16(scale * dQacc), 8 elements per thread (dQacc rows padded per head);
 // with more accumulators, dq = bf16(scale * (((dQacc + dQacc_1) + dQacc_2) + ...)), always in
-// that order.
+// that order.  The grid's y index walks the heads, x the head's N x D / 8 groups of 8.
 // ------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ acc,
@@ -183,10 +193,15 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
                                                            float scale, long long n8, int N, int npad,
                                                            const int* __restrict__ cu_q, int nseq, long long rows_pad) {
   pdl_wait();   // launched as a programmatic dependent of the main kernel
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / (D / 8), bh = row / N, rr = row - bh * N;
-    const long long arow = cu_q ? bh * rows_pad + rr + 128LL * seq_of(cu_q, nseq, (int)rr) : bh * npad + rr;
-    const long long src = (arow * D) / 8 + i % (D / 8);
+  constexpr int G8 = D / 8;                  // groups of 8 per row (a power of two)
+  const long long n_heads = n8 / ((long long)N * G8);
+  const int per_head = N * G8;
+  for (long long bh = blockIdx.y; bh < n_heads; bh += gridDim.y)
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < per_head; e += gridDim.x * blockDim.x) {
+    const int rr = e / G8, c8 = e & (G8 - 1);
+    const long long i = bh * per_head + e;
+    const long long arow = cu_q ? bh * rows_pad + rr + 128LL * seq_of(cu_q, nseq, rr) : bh * npad + rr;
+    const long long src = arow * G8 + c8;
     float4 a = reinterpret_cast<const float4*>(acc)[2 * src];
     float4 b = reinterpret_cast<const float4*>(acc)[2 * src + 1];
     for (int x = 0; x < n_extra; ++x) {
@@ -932,9 +947,10 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   float* const extra = det_k > 1 ? p.dq_acc2 : nullptr;
   const long long extra_stride = (long long)(align256((size_t)p.B * p.Hq * nq * 128 * D * 4) / 4);
   {
-    const long long blocks = std::max((rows + 15) / 16, ((long long)n_sem + 255) / 256);
-    if (blocks > 0) {
-      e = launch_pdl(bwd_preprocess_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, s,
+    const long long n_heads = p.N > 0 ? rows / p.N : 0;
+    const unsigned gx = (unsigned)((p.N + 15) / 16), gy = (unsigned)std::min<long long>(n_heads, 65535);
+    if (rows > 0) {
+      e = launch_pdl(bwd_preprocess_kernel<D>, dim3(gx, gy), dim3(256), 0, s,
                      static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.delta, p.lse2,
                      p.dq_acc, extra, det_k - 1, extra_stride, p.sem, rows, p.N, nq * 128, n_sem, cu_q, p.B,
                      rows_pad);
@@ -982,9 +998,13 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   }
   {
     const long long n8 = rows * D / 8;
-    const long long blocks = std::min<long long>((n8 + 255) / 256, (long long)sms * 8);
-    if (blocks > 0) {
-      return launch_pdl(bwd_convert_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, s,
+    const long long n_heads = p.N > 0 ? rows / p.N : 0;
+    const long long per_head = (long long)p.N * (D / 8);
+    const unsigned gy = (unsigned)std::min<long long>(n_heads, 65535);
+    const unsigned gx = (unsigned)std::max<long long>(1, std::min<long long>((per_head + 255) / 256,
+                                                                             ((long long)sms * 16 + gy - 1) / gy));
+    if (n8 > 0) {
+      return launch_pdl(bwd_convert_kernel<D>, dim3(gx, gy), dim3(256), 0, s,
                         static_cast<const float*>(p.dq_acc), static_cast<const float*>(extra), det_k - 1,
                         extra_stride, static_cast<uint16_t*>(p.dq), p.scale, n8, p.N, nq * 128, cu_q, p.B,
                         rows_pad);
