@@ -690,13 +690,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float4* nd4 = reinterpret_cast<const float4*>(vec_d + h * 64);
       uint32_t pk[32];
       {
+        // Two halves of 32 columns: the second half's load is in flight while the first
+        // half's probabilities are computed, and the first half's P is stored meanwhile.
         uint32_t u[64];
         tmem_ld32(tS + lane_off + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tS + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        reg_fence_b(u);
+        reg_fence_b(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
+          if (i == 32) {
+            tmem_st16(tS + lane_off + h * 64, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+            tmem_wait_ld();
+            reg_fence_b(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+          }
           const float4 nl = nl4[i >> 2];
           float x0, x1, x2, x3;
           ffma2(x0, x1, __uint_as_float(u[i]), __uint_as_float(u[i + 1]), a.c, a.c, nl.x, nl.y);
@@ -712,7 +719,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[(i >> 1) + 1] = pack_bf16x2(p2, p3);
         }
       }
-      tmem_st32(tS + lane_off + h * 64, pk);
+      tmem_st16(tS + lane_off + h * 64 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(W_P));
@@ -722,13 +729,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!warp_wait_b(BAR(W_DP), it & 1, wc)) { ok = false; break; }
       tc_fence_after();
       {
+        // As above: the second 32 columns of dP^T load while the first are turned into dS^T.
         uint32_t u[64];
         tmem_ld32(tdP + lane_off + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tdP + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        reg_fence_b(u);
+        reg_fence_b(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tdP + lane_off + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
+          if (cc == 1) {
+            tmem_wait_ld();
+            reg_fence_b(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+          }
           uint32_t out[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
