@@ -42,13 +42,21 @@ struct FwdCfg {
   static constexpr int NCH = D / 64;                          // 64-column (128-byte) chunks
   static constexpr uint32_t CHUNK = 128 * 128;                // bytes of one 128 x 64 bf16 box
   static constexpr uint32_t TILE = CHUNK * NCH;               // one 128 x D bf16 tile
-  static constexpr int NS = (D == 128) ? 4 : 8;               // K/V ring slots
+  // K and V tiles through rings of their own: K_j is last read by S_1(j), at the end of
+  // block j, and first read by S_0(j) after PV_0(j - 1), so with one ring of four slots its
+  // load could start only one block ahead and (≈ 2800 cycles from L2 under load, traced)
+  // arrived late; three K slots start it two blocks ahead.  V_j is read one block after
+  // its load can start with two slots.
+  static constexpr int NK = (D == 128) ? 3 : 4;               // K ring slots
+  static constexpr int NV = (D == 128) ? 2 : 4;               // V ring slots
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_RING = 2 * TILE;
-  static constexpr uint32_t OFF_CTRL = OFF_RING + NS * TILE;
-  // control block: barriers then per-row buffers
-  static constexpr uint32_t CTRL_BYTES = 256 + 8 * 128 * 4 + 64;
+  static constexpr uint32_t OFF_KRING = 2 * TILE;
+  static constexpr uint32_t OFF_VRING = OFF_KRING + NK * TILE;
+  static constexpr uint32_t OFF_CTRL = OFF_VRING + NV * TILE;
+  // control block: barriers, then alpha[2][128], then the TMEM address and abort flag
+  static constexpr uint32_t CTRL_BYTES = 256 + 2 * 128 * 4 + 64;
   static constexpr uint32_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
 };
@@ -62,9 +70,10 @@ enum {
   B_REL = 7,      // +(group & 1): K/V slots of release group j (K_j, V_(j-1)) are free
   B_OFULL = 9,    // +t: the tile's last PV product has completed (one phase)
   B_DONE = 11,
-  B_FULL = 12,    // +slot (up to 8)
+  B_KFULL = 12,   // +K slot (up to 4)
+  B_VFULL = 16,   // +V slot (up to 4)
   B_EPI = 28,     // +t: the tile's O rows are staged in shared memory
-  B_FIN = 30,     // +t: final row statistics (m, l) written (one phase only)
+  B_FIN = 30,     // +t: final row statistics (m, l, lq) in TMEM (one phase only)
   B_COUNT = 32
 };
 
@@ -206,10 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = smem_u32(ctrl);
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   float* alpha_buf = reinterpret_cast<float*>(ctrl + 256);        // [2][128]
-  float* m_fin = alpha_buf + 256;                                 // [2][128]
-  float* l_fin = m_fin + 256;                                     // [2][128]
-  float* lq_fin = l_fin + 256;                                    // [2][128]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lq_fin + 256);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(alpha_buf + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -257,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_EPI + 1), 128);
     mbar_init(BAR(B_FIN + 0), 128);
     mbar_init(BAR(B_FIN + 1), 128);
-    for (int s = 0; s < C::NS; ++s) mbar_init(BAR(B_FULL + s), 1);
+    for (int s = 0; s < C::NK; ++s) mbar_init(BAR(B_KFULL + s), 1);
+    for (int s = 0; s < C::NV; ++s) mbar_init(BAR(B_VFULL + s), 1);
     *abort_flag = 0;
     fence_mbar_init();
     // Thread 0 is also the producer: its first loads (the Q tiles, K_0 and V_0, which need no
@@ -272,10 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (nmax > 0 && !p.test_skip_first_kv) {
       for (int which = 0; which < 2; ++which) {
-        mbar_arrive_expect_tx(BAR(B_FULL + which), C::TILE);
+        const uint32_t bar = BAR(which ? B_VFULL : B_KFULL);
+        mbar_arrive_expect_tx(bar, C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sbase + C::OFF_RING + which * C::TILE + c * C::CHUNK, which ? &tm_v : &tm_k, c * 64,
-                      T.krow0 + T.j0 * 128, T.bkv, BAR(B_FULL + which));
+          tma_load_3d(sbase + (which ? C::OFF_VRING : C::OFF_KRING) + c * C::CHUNK, which ? &tm_v : &tm_k, c * 64,
+                      T.krow0 + T.j0 * 128, T.bkv, bar);
       }
     }
   }
@@ -300,41 +308,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_o);
-      // The Q tiles and ring indices 0 and 1 (K_0, V_0) were issued before the CTA-wide
-      // barrier.  next_idx: one past the last ring index handed to the TMA unit.  skip_idx: a
-      // ring index deliberately never loaded (test hook for the bounded-wait path: the first
-      // K and V are then both skipped), or -1.
-      const int skip_idx = p.test_skip_first_kv ? 0 : -1;
-      int next_idx = nmax > 0 ? 2 : 0;
+      // The Q tiles, K_0 and V_0 were issued before the CTA-wide barrier.  K_k goes to K slot
+      // k mod NK once release k - NK (the end of block k - NK) has freed it; V_k to V slot
+      // k mod NV once release k - NV + 1 has (V_(k-NV)'s last reader is the PV issued in block
+      // k - NV + 1).  The loads go out in the order of the releases they wait for.  The test
+      // hook skips K_0 and V_0 (the bounded-wait path).
+      const bool skip0 = p.test_skip_first_kv;
+      int nk = nmax > 0 ? 1 : 0, nv = nk;
       bool ok = true;
-      for (int j = 1; j < nmax && ok; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const int idx = 2 * j + which, slot = idx % C::NS;
-          if (idx >= C::NS) {
-            // The slot's previous occupant (ring index idx - NS) is released with group g.
-            const int g = (idx - C::NS + 1) / 2;
-            if (!mbar_wait(BAR(B_REL + (g & 1)), (g >> 1) & 1, wc)) {
-              ok = false;
-              break;
-            }
-          }
-          next_idx = idx + 1;
-          if (idx == skip_idx) continue;
-          mbar_arrive_expect_tx(BAR(B_FULL + slot), C::TILE);
-          const CUtensorMap* tm = which ? &tm_v : &tm_k;
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64,
-                        T.krow0 + (T.j0 + j) * 128, T.bkv, BAR(B_FULL + slot));
+      while (ok && (nk < nmax || nv < nmax)) {
+        const int gk = nk < nmax ? (nk >= C::NK ? nk - C::NK : -1) : 0x7fffffff;
+        const int gv = nv < nmax ? (nv >= C::NV ? nv - C::NV + 1 : -1) : 0x7fffffff;
+        const bool is_k = gk <= gv;
+        const int g = is_k ? gk : gv;
+        if (g >= 0 && !mbar_wait(BAR(B_REL + (g & 1)), (g >> 1) & 1, wc)) {
+          ok = false;
+          break;
         }
+        const int k = is_k ? nk : nv;
+        const uint32_t bar = is_k ? BAR(B_KFULL + k % C::NK) : BAR(B_VFULL + k % C::NV);
+        const uint32_t dst = sbase + (is_k ? C::OFF_KRING + (k % C::NK) * C::TILE : C::OFF_VRING + (k % C::NV) * C::TILE);
+        mbar_arrive_expect_tx(bar, C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(dst + c * C::CHUNK, is_k ? &tm_k : &tm_v, c * 64, T.krow0 + (T.j0 + k) * 128, T.bkv, bar);
+        if (is_k) ++nk;
+        else ++nv;
       }
       if (!ok) {
         // Let the copies still in flight land before the CTA's shared memory goes away:
-        // only the last NS ring indices can be outstanding.
+        // only the last NK K loads and NV V loads can be outstanding.
         const unsigned long long t0 = globaltimer_ns();
-        for (int idx = max(0, next_idx - C::NS); idx < next_idx; ++idx) {
-          if (skip_idx == 0 && idx < 2) continue;
-          const uint32_t bar = BAR(B_FULL + idx % C::NS), par = (idx / C::NS) & 1;
-          while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 < p.wait_ns) {
+        for (int k = max(0, nk - C::NK); k < nk; ++k) {
+          if (skip0 && k == 0) continue;
+          while (!mbar_try_wait(BAR(B_KFULL + k % C::NK), (k / C::NK) & 1) && globaltimer_ns() - t0 < p.wait_ns) {
+          }
+        }
+        for (int k = max(0, nv - C::NV); k < nv; ++k) {
+          if (skip0 && k == 0) continue;
+          while (!mbar_try_wait(BAR(B_VFULL + k % C::NV), (k / C::NV) & 1) && globaltimer_ns() - t0 < p.wait_ns) {
           }
         }
       }
@@ -345,15 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(BAR(B_Q), 0, wc);
       tc_fence_after();
       for (int j = 0; j <= nmax && ok; ++j) {
-        const int kidx = 2 * j, kslot = kidx % C::NS;
-        const int vidx = 2 * (j - 1) + 1, vslot = (vidx + C::NS) % C::NS;
-        if (j < nmax && !mbar_wait(BAR(B_FULL + kslot), (kidx / C::NS) & 1, wc)) { ok = false; break; }
-        if (j >= 1 && !mbar_wait(BAR(B_FULL + vslot), (vidx / C::NS) & 1, wc)) { ok = false; break; }
+        const int kslot = j % C::NK, vslot = (j + C::NV - 1) % C::NV;   // K_j, V_(j-1)
+        if (j < nmax && !mbar_wait(BAR(B_KFULL + kslot), (j / C::NK) & 1, wc)) { ok = false; break; }
+        if (j >= 1 && !mbar_wait(BAR(B_VFULL + vslot), ((j - 1) / C::NV) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         // Descriptor low words built once per block and advanced by (offset / 16); the high
         // words are constants.
-        const uint32_t klo = sdesc_sw128_lo(sbase + C::OFF_RING + kslot * C::TILE, 16);
-        const uint32_t vlo = sdesc_sw128_lo(sbase + C::OFF_RING + vslot * C::TILE, C::CHUNK);
+        const uint32_t klo = sdesc_sw128_lo(sbase + C::OFF_KRING + kslot * C::TILE, 16);
+        const uint32_t vlo = sdesc_sw128_lo(sbase + C::OFF_VRING + vslot * C::TILE, C::CHUNK);
         constexpr uint32_t HI = sdesc_sw128_hi(1024);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -387,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(BAR(B_REL + (j & 1)));   // releases K_j and V_(j-1) together
+        mma_commit(BAR(B_REL + (j & 1)));   // release j: K_j's and V_(j-1)'s slots
       }
       // Drain: every MMA issued above completes before TMEM is released.
       mma_commit(BAR(B_DONE));
@@ -485,11 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(BAR(B_PFULL + t));
     }
-    // A barrier of its own: arriving on B_STATS again here could complete that
-    // barrier's last two phases before the correction group waits on the first.
-    m_fin[t * 128 + row] = m;
-    l_fin[t * 128 + row] = l;
-    lq_fin[t * 128 + row] = lq;
+    // The row's final statistics go to TMEM columns 64-67 of this tile's S, dead once the
+    // last P (columns 0-63) is written, for the correction group's epilogue.  A barrier of
+    // its own: arriving on B_STATS again here could complete that barrier's last two phases
+    // before the correction group waits on the first.
+    {
+      const uint32_t st[4] = {__float_as_uint(m), __float_as_uint(l), __float_as_uint(lq), 0u};
+      tmem_st4(tS + 64, st);
+      tmem_wait_st();
+    }
+    tc_fence_before();
     mbar_arrive(BAR(B_FIN + t));
   } else {
     if constexpr (D == 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
@@ -539,8 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(BAR(B_FIN + t), 0, wc)) { ok = false; break; }
       if (!warp_wait(BAR(B_OFULL + t), 0, wc)) { ok = false; break; }
       tc_fence_after();
-      const float mrow = m_fin[t * 128 + row], lrow = l_fin[t * 128 + row];
-      const float inv = 1.f / lq_fin[t * 128 + row];
+      uint32_t fin[4];
+      tmem_ld4(tmem + lane_off + uint32_t(t * 128) + 64u, fin);
+      tmem_wait_ld();
+      reg_fence(fin);
+      const float mrow = __uint_as_float(fin[0]), lrow = __uint_as_float(fin[1]), lq_row = __uint_as_float(fin[2]);
+      const float inv = 1.f / lq_row;
       const uint32_t tO = tmem + lane_off + 256u + uint32_t(t * D);
       if constexpr (MODE == 1) {
         // This key split's partial result: O / lq (0 where the row saw no key) and LSE, fp32,
@@ -548,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int unit = blockIdx.x / p.kv_splits, sp = blockIdx.x % p.kv_splits;
         const size_t slot = (size_t)sp * (p.B * p.Hkv) + unit;
         const bool real = row < p.g * p.N;
-        const float lqr = lq_fin[t * 128 + row];
+        const float lqr = lq_row;
         const float invp = lqr > 0.f ? 1.f / lqr : 0.f;
         float* dst = p.part_o + (slot * 128 + row) * D;
         uint32_t r[32];
