@@ -38,17 +38,23 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Deterministic mode splits a tile's contributions into up to this many classes, each with
 // its own counter and accumulator (see the kernel).
-constexpr int kDetMaxClasses = 2;
+constexpr int kDetMaxClasses = 4;
+// Classes used for a non-causal head of nq query tiles (causal heads use one).  Measured on
+// GB300 (B2 H16 d128, deterministic): four classes instead of two take N = 8192 from 3.27 to
+// 3.08 ms and N = 16384 from 6.00 to 5.85 ms, but N = 2048 from 0.472 to 0.496 ms (the two
+// extra accumulators' zeroing and reading weigh more on a short call).
+static int det_classes(int nq) { return nq >= 64 ? 4 : 2; }
 
 // Layout: dQacc [B, Hq, ceil(N/128)*128, d] fp32, delta and LSE2 [B, Hq, N] fp32, and when
-// deterministic the counters [kDetMaxClasses][B, Hq, ceil(N/128)] and kDetMaxClasses - 1
-// more accumulators shaped as dQacc, each starting on a 256-byte boundary.
+// deterministic the counters [kDetMaxClasses][B, Hq, ceil(N/128)] and det_classes - 1 more
+// accumulators shaped as dQacc, each starting on a 256-byte boundary.
 size_t bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int deterministic) {
   (void)Hkv;
   const size_t rows = (size_t)B * Hq * N;
-  const size_t nq = (size_t)B * Hq * ((N + 127) / 128);
+  const int tiles = (N + 127) / 128;
+  const size_t nq = (size_t)B * Hq * tiles;
   size_t n = align256(nq * 128 * d * 4) + 2 * align256(rows * 4);
-  if (deterministic) n += align256(kDetMaxClasses * nq * 4) + (kDetMaxClasses - 1) * align256(nq * 128 * d * 4);
+  if (deterministic) n += align256(kDetMaxClasses * nq * 4) + (det_classes(tiles) - 1) * align256(nq * 128 * d * 4);
   return n;
 }
 
@@ -314,7 +320,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 struct BwdKernelArgs {
   int B, Hq, Hkv, N, g, nq, nkb, causal, deterministic;
   int det_rotate;   // deterministic with the rotating per-tile order (see the kernel)
-  int det_k;        // deterministic: contribution classes (1 or 2), one accumulator each
+  int det_k;        // deterministic: contribution classes (1, 2 or 4), one accumulator each
   int det_releaser; // deterministic: warp 2 passes the counters on (else the drain leader)
   float c, scale;
   const float* lse2;
@@ -827,7 +833,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_store_3d(&tm_dk, sbase + C::OFF_STAGE + C::TILE + c * C::CHUNK, c * 64, k0 + n * 128, bkv);
           }
           tma_store_commit();
-          tma_store_wait_all();
+          tma_store_wait_read();   // the CTA may exit once the stores have read shared memory
         }
       }
     }
@@ -948,13 +954,14 @@ static cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, cudaStream
   // The rotating deterministic order (see the kernel) needs every key block of a head on
   // the GPU at once: enabled when a head's blocks take at most half the SMs.
   const bool rotate = !VL && DET && !p.causal && 2 * nq <= sms;
-  // Deterministic, measured on GB300 (B2 H16 d128): two classes cut the non-causal cost
+  // Deterministic, measured on GB300 (B2 H16 d128): two classes (four from N = 8192 on, see
+  // det_classes) cut the non-causal cost
   // (N = 8192, rotating: 3.60 -> 3.27 ms; N = 16384, shared: 6.77 -> 6.00 ms, both with the
   // releaser; four classes gained at most 6 % more and lost 5 % at N = 2048) but not the
   // causal one, whose second accumulator only costs its zeroing and reading; the releaser
   // helps wherever it is used here (causal N = 8192: 1.71 -> 1.49 ms) but, with one class,
   // not the non-causal shared order (N = 16384: 6.77 -> 7.47 ms).
-  const int det_k = DET && !VL && !p.causal ? 2 : 1;
+  const int det_k = DET && !VL && !p.causal ? det_classes(nq) : 1;
   const int det_rel = DET && (det_k > 1 || p.causal) ? 1 : 0;
   float* const extra = det_k > 1 ? p.dq_acc2 : nullptr;
   const long long extra_stride = (long long)(align256((size_t)p.B * p.Hq * nq * 128 * D * 4) / 4);

@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
           tma_store_3d(&tm_dk, sbase + C::OFF_K + 2 * C::KCH + c * C::KCH, c0 + c * 64, n * 128, bkv);
         }
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();   // the CTA may exit once the stores have read shared memory
       }
     }
   } else {

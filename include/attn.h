@@ -239,8 +239,9 @@ int attn_set_varlen_order(int longest_first);
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ accumulator
  * [B,Hq,ceil(N/128)*128,d] with each head's rows padded to whole 128-row tiles,
  * rowsum(dO o O) and LSE*log2(e) [B,Hq,N]; when deterministic, ordering counters and,
- * for d <= 128, a second fp32 accumulator of the same shape).  0 when there is nothing
- * to do.  Returns (size_t)-1 for invalid sizes.
+ * for d <= 128, more fp32 accumulators of the same shape: one when N <= 8064, three for
+ * longer sequences).  0 when there is nothing to do.  Returns (size_t)-1 for invalid
+ * sizes.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int deterministic);
 

@@ -92,14 +92,21 @@ def test_bwd_workspace_and_errors(lib):
                       FAKE, 16, None)
     assert rc == -4                          # workspace too small
     # d <= 128: dQ accumulator (rows padded to 128-row tiles), D and LSE2; deterministic adds
-    # two counter sets per (head, 128-row tile) and a second accumulator.  The size covers
+    # four counter sets per (head, 128-row tile) and a second accumulator.  The size covers
     # the 64-row-tile layout too, which is never larger at these sizes.
     al = lambda x: (x + 255) // 256 * 256
     B, Hq, N, d = 2, 4, 300, 128
     acc = al(B * Hq * 384 * d * 4)
     base = acc + 2 * al(B * Hq * N * 4)
     assert lib.attn_bwd_workspace_size(B, Hq, 2, N, d, 0) == base
-    assert lib.attn_bwd_workspace_size(B, Hq, 2, N, d, 1) == base + al(2 * B * Hq * 3 * 4) + acc
+    assert lib.attn_bwd_workspace_size(B, Hq, 2, N, d, 1) == base + al(4 * B * Hq * 3 * 4) + acc
+    # from 64 query tiles per head (N > 8064) on, three more accumulators
+    B, Hq, N, d = 1, 2, 8065, 64
+    acc = al(B * Hq * 64 * 128 * d * 4)
+    base = acc + 2 * al(B * Hq * N * 4)
+    assert lib.attn_bwd_workspace_size(B, Hq, 2, N, d, 1) == base + al(4 * B * Hq * 64 * 4) + 3 * acc
+    assert lib.attn_bwd_workspace_size(B, Hq, 2, 8064, d, 1) == (
+        al(B * Hq * 8064 * d * 4) + 2 * al(B * Hq * 8064 * 4) + al(4 * B * Hq * 63 * 4) + al(B * Hq * 8064 * d * 4))
     # wide heads (192, 256): dQ accumulator rows padded to whole 64-row tiles, counters per
     # (head, 64-row tile, column half) when deterministic
     for d in (192, 256):
