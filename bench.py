@@ -589,6 +589,10 @@ def _case_table():
         "fwd_d128_N8192_persistent": ("forward B2 H16 N8192 d128 non-causal, persistent kernel",
                                       fwd(2, 16, 16, 8192, 128, False, persistent=True)),
         "fwd_d64_N8192_noncausal": ("forward B2 H16 N8192 d64 non-causal", fwd(2, 16, 16, 8192, 64, False)),
+        "fwd_d64_N8192_causal": ("forward B2 H16 N8192 d64 causal", fwd(2, 16, 16, 8192, 64, True)),
+        "fwd_d64_N4096_noncausal": ("forward B4 H16 N4096 d64 non-causal", fwd(4, 16, 16, 4096, 64, False)),
+        "fwd_d64_N2048_noncausal": ("forward B4 H16 N2048 d64 non-causal", fwd(4, 16, 16, 2048, 64, False)),
+        "fwd_d64_N16384_noncausal": ("forward B1 H16 N16384 d64 non-causal", fwd(1, 16, 16, 16384, 64, False)),
         "fwd_d256_N8192_noncausal": ("forward B2 H16 N8192 d256 non-causal (one-tile kernel)",
                                      fwd(2, 16, 16, 8192, 256, False, seed=9)),
         "fwd_gqa8_N8192_causal_outliers": ("forward B2 Hq32 Hkv8 N8192 d128 causal, outlier inputs",
