@@ -104,3 +104,28 @@ def test_grouped_decode_two_tile_kernel(A, shape, causal):
     assert A.attn_device_status(True) == 0
     O, L = oracle.attn_fwd_kv(q, x["k"], x["v"], causal, scale)
     check_fwd(o.float().cpu().numpy(), lse.cpu().numpy(), O, L, f"two-tile {shape} causal={causal}")
+
+
+# Larger grouped-decode shapes, compared in full: 40 groups of 10 key blocks, 4 groups of 71
+# blocks with 16 queries each, and the decode benchmark's B8 Hq32 Hkv8 Nk8192.
+LARGER = [  # B, Hq, Hkv, Nq, Nk, d
+    (5, 32, 8, 1, 1280, 128),
+    (2, 8, 2, 16, 9000, 128),
+    (8, 32, 8, 1, 8192, 128),
+]
+
+
+@pytest.mark.parametrize("shape", LARGER, ids=lambda s: "B%dHq%dHkv%dNq%dNk%dd%d" % s)
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_decode_larger(A, shape, causal):
+    B, Hq, Hkv, Nq, Nk, d = shape
+    x = make_inputs(640 + Nq + Nk, B, Hq, Hkv, Nk, d)
+    q = x["q"][:, :, Nk - Nq:].contiguous()
+    scale = default_scale(d)
+    dev = torch.device("cuda")
+    assert A.attn_fwd_kv_workspace_size(B, Hq, Hkv, Nq, Nk, d) > 0
+    o, lse = A.attn_fwd_kv(q.to(dev), x["k"].to(dev), x["v"].to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert A.attn_device_status(True) == 0
+    O, L = oracle.attn_fwd_kv(q, x["k"], x["v"], causal, scale)
+    check_fwd(o.float().cpu().numpy(), lse.cpu().numpy(), O, L, f"larger {shape} causal={causal}")
