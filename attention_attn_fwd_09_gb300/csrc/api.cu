@@ -328,6 +328,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
     else if (units < sms && 2 * units <= sms) p.split_from = 0;
   }
   long long grid = p.split_from + 2 * (units - p.split_from);
+  p.prefetch_ahead = std::max(1, s->sms);
   p.q_tile_bytes = (unsigned)((d / 64) * 128 * 128);
   // One query tile per CTA (fwd_wide.cu): always for d > 128, and for d = 128 when chosen.
   const bool wide = d > 128 || (d == 128 && !pack && g_one_tile_d128.load());

@@ -226,6 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   // CTAs past split_from each take one tile of a unit (the other half of the unit goes to
   // the next CTA); the lone tile always sits in slot 0.
+  auto cta_tiles = [&](int cta) -> Tiles {
+    if (cta < p.split_from) return map_unit(p, cta);
+    const int k = cta - p.split_from;
+    Tiles U = map_unit(p, p.split_from + k / 2);
+    if (k & 1) {
+      U.n[0] = U.n[1];
+      U.row0[0] = U.row0[1];
+      U.bh[0] = U.bh[1];
+    }
+    U.n[1] = 0;
+    return U;
+  };
   Tiles T;
   if constexpr (MODE == 2) {
     // CTAs past the table's records have no work: they leave before touching barriers or
@@ -234,17 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     T = map_unit_varlen(p, p.vl_units[blockIdx.x]);
   } else if constexpr (MODE == 1) {
     T = map_unit_grouped(p, blockIdx.x);
-  } else if ((int)blockIdx.x < p.split_from) {
-    T = map_unit(p, blockIdx.x);
   } else {
-    const int k = (int)blockIdx.x - p.split_from;
-    T = map_unit(p, p.split_from + k / 2);
-    if (k & 1) {
-      T.n[0] = T.n[1];
-      T.row0[0] = T.row0[1];
-      T.bh[0] = T.bh[1];
-    }
-    T.n[1] = 0;
+    T = cta_tiles(blockIdx.x);
   }
   const int nmax = max(T.n[0], T.n[1]);
   WaitCtl wc{p.wait_ns, p.status, abort_flag};
@@ -333,6 +336,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(dst + c * C::CHUNK, is_k ? &tm_k : &tm_v, c * 64, T.krow0 + (T.j0 + k) * 128, T.bkv, bar);
         if (is_k) ++nk;
         else ++nv;
+      }
+      // The CTA one wave later (blockIdx + the SM count) starts about when this one ends:
+      // bring its Q tiles and first K, V tiles into L2 now, so that its first loads do not
+      // wait on HBM.
+      if constexpr (MODE == 0) {
+        const int nxt = (int)blockIdx.x + p.prefetch_ahead;
+        if (ok && p.prefetch_ahead > 0 && nxt < (int)gridDim.x) {
+          const Tiles U = cta_tiles(nxt);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if ((t ? U.n[1] : U.n[0]) == 0) continue;
+            for (int c = 0; c < C::NCH; ++c)
+              tma_prefetch_l2_3d(&tm_q, c * 64, t ? U.row0[1] : U.row0[0], t ? U.bh[1] : U.bh[0]);
+          }
+          if (max(U.n[0], U.n[1]) > 0) {
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_prefetch_l2_3d(&tm_k, c * 64, U.krow0 + U.j0 * 128, U.bkv);
+              tma_prefetch_l2_3d(&tm_v, c * 64, U.krow0 + U.j0 * 128, U.bkv);
+            }
+          }
+        }
       }
       if (!ok) {
         // Let the copies still in flight land before the CTA's shared memory goes away:

@@ -42,6 +42,7 @@ struct FwdParams {
   int units_per_row;       // CTAs per query-row slot (see fwd.cu unit mapping)
   int n_rowslots;          // query-row slots per head (pair) sequence
   int split_from;          // units >= split_from run as two one-tile CTAs (the last, partial wave)
+  int prefetch_ahead;      // > 0: a CTA prefetches into L2 the first tiles of CTA blockIdx + this
   // Grouped decode mode (queries after a key cache, g * N <= 128): one CTA per (K/V head,
   // key split) with one tile holding the group's g query heads x N queries; each CTA writes
   // a normalised partial O and LSE for its key range, merged by launch_fwd_merge.
