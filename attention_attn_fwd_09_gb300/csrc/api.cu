@@ -568,6 +568,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   }
   const long long grid = p.split_from + 2 * (units - p.split_from);
   if (grid > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+  p.prefetch_ahead = std::max(1, s->sms);
   const Fp8Scales sc{q_scale, k_scale, v_scale};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_fwd_fp8(maps, p, sc, (int)grid, st);

@@ -193,19 +193,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int wg = warp >> 2;
-  F8Tiles T;
-  if ((int)blockIdx.x < p.split_from) {
-    T = f8_unit(p, blockIdx.x);
-  } else {
-    const int k = (int)blockIdx.x - p.split_from;
-    T = f8_unit(p, p.split_from + k / 2);
+  auto f8_cta = [&](int cta) -> F8Tiles {
+    if (cta < p.split_from) return f8_unit(p, cta);
+    const int k = cta - p.split_from;
+    F8Tiles U = f8_unit(p, p.split_from + k / 2);
     if (k & 1) {
-      T.n[0] = T.n[1];
-      T.row0[0] = T.row0[1];
-      T.bh[0] = T.bh[1];
+      U.n[0] = U.n[1];
+      U.row0[0] = U.row0[1];
+      U.bh[0] = U.bh[1];
     }
-    T.n[1] = 0;
-  }
+    U.n[1] = 0;
+    return U;
+  };
+  const F8Tiles T = f8_cta(blockIdx.x);
   const int nmax = max(T.n[0], T.n[1]);
   WaitCtl wc{p.wait_ns, p.status, abort_flag};
 
@@ -277,6 +277,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           mbar_arrive_expect_tx(BAR(E_V8FULL + vs), C::T8);
           tma_load_3d(sbase + C::OFF_V8 + vs * C::T8, &tm_v, 0, j * 128, T.bkv, BAR(E_V8FULL + vs));
           v_issued = j + 1;
+        }
+        // The CTA one wave later (blockIdx + the SM count) starts about when this one ends:
+        // bring its Q tiles and first K, V tiles into L2 now.
+        const int nxt = (int)blockIdx.x + p.prefetch_ahead;
+        if (ok && p.prefetch_ahead > 0 && nxt < (int)gridDim.x) {
+          const F8Tiles U = f8_cta(nxt);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if ((t ? U.n[1] : U.n[0]) > 0) tma_prefetch_l2_3d(&tm_q, 0, t ? U.row0[1] : U.row0[0], t ? U.bh[1] : U.bh[0]);
+          if (max(U.n[0], U.n[1]) > 0) {
+            tma_prefetch_l2_3d(&tm_k, 0, 0, U.bkv);
+            tma_prefetch_l2_3d(&tm_v, 0, 0, U.bkv);
+          }
         }
         if (!ok) {
           // Let the copies still in flight land before the shared memory goes away.
