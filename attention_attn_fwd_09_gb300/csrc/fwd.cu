@@ -10,7 +10,8 @@
 //     row blocks of one head, or, for grouped heads, the same row block of two query
 //     heads that share one K/V head, so every K/V tile loaded serves both (the MQA K/V
 //     reuse of the reverse-engineering page);
-//   * warp 0 is the TMA producer (Q tiles once, K/V tiles through a ring of slots);
+//   * warp 0 is the TMA producer (Q tiles once, K and V tiles through rings of their own,
+//     then an L2 prefetch of the first tiles of the CTA one wave later);
 //   * warp 1 issues tcgen05.mma: S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with P read
 //     from TMEM (S and P share columns, "Hotelren FA4 summary" section 4.2 item 1);
 //   * warpgroups 1 and 2 are the softmax of tile 0 and tile 1: while one does its
@@ -18,9 +19,10 @@
 //   * warpgroup 3 is the correction group: it rescales O in TMEM only when a row's
 //     running maximum grew by more than tau (section 3.3, tau = 8 in log2 units), and
 //     does the epilogue: O / l -> bf16 -> shared memory -> TMA store, plus the LSE;
-//   * exponentials: each softmax thread sends a fixed subset of its elements through
+//   * exponentials: each softmax thread can send a fixed subset of its elements through
 //     the FMA-pipe cubic (exp2poly.cuh) and the rest through MUFU.EX2 (section 3.2,
-//     mixed execution).
+//     mixed execution); the default (POLY = 0) sends all of them to MUFU.EX2, which
+//     measured faster on this GPU.
 //
 // TMEM (512 columns, fp32): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D).
 // P_t (bf16 pairs) overwrites the first 64 columns of S_t.
