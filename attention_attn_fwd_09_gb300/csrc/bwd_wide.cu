@@ -140,6 +140,7 @@ struct BwArgs {
   int* sem;           // [B, Hq, nq64, column blocks] when deterministic
   unsigned long long wait_ns;
   int* status;
+  int prefetch_ahead;   // > 0: the producer prefetches into L2 the first tiles of CTA blockIdx + this
 };
 
 template <int D, bool DET>
@@ -244,6 +245,25 @@ __global__ void __launch_bounds__(kBwThreads, 1)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sbase + C::OFF_Q + st * C::QT + c * C::QCH, &tm_q, c * 64, m * 64, bh, BAR(X_QFULL + st));
           q_next = it + 1;
+        }
+        // The CTA one wave later (blockIdx + the SM count) starts about when this one ends:
+        // bring its K and V tiles and its first dO and Q tiles into L2 now (atomic dQ only,
+        // as in the 128-row kernel).
+        if constexpr (!DET) {
+          const int nxt = (int)blockIdx.x + a.prefetch_ahead;
+          if (ok && a.prefetch_ahead > 0 && nxt < (int)gridDim.x) {
+            const int rest2 = C::NHALF == 2 ? (nxt >> 1) : nxt;
+            const int bkv2 = a.causal ? rest2 % nbkv : rest2 / a.nkb;
+            const int n2 = a.causal ? rest2 / nbkv : rest2 % a.nkb;
+            const int m2 = a.causal ? 2 * n2 : (a.nq64 > 0 ? (2 * n2) % a.nq64 : 0);
+            const int bh2 = (bkv2 / a.Hkv) * a.Hq + (bkv2 % a.Hkv) * a.g;
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_prefetch_l2_3d(&tm_k, c * 64, n2 * 128, bkv2);
+              tma_prefetch_l2_3d(&tm_v, c * 64, n2 * 128, bkv2);
+              tma_prefetch_l2_3d(&tm_do, c * 64, m2 * 64, bh2);
+              tma_prefetch_l2_3d(&tm_q, c * 64, m2 * 64, bh2);
+            }
+          }
         }
         if (!ok) {
           const unsigned long long t0 = globaltimer_ns();
@@ -677,6 +697,7 @@ cudaError_t launch_wide_t(const BwdMaps& m, const BwdParams& p, cudaStream_t s) 
     a.c = p.c; a.scale = p.scale;
     a.lse2 = p.lse2; a.delta = p.delta; a.dq_acc = p.dq_acc; a.sem = p.sem;
     a.wait_ns = p.wait_ns; a.status = p.status;
+    a.prefetch_ahead = sms;
     const long long grid = (long long)p.B * p.Hkv * a.nkb * BwCfg<D>::NHALF;
     if (grid > 0) {
       kern<<<(unsigned)grid, kBwThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);

@@ -276,6 +276,21 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tma_load_3d(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK, tm, c * 64, T.krow0 + (T.j0 + j) * 128,
                       T.bkv, BAR(V_FULL + slot));
       }
+      // The CTA one wave later (blockIdx + the SM count) starts about when this one ends:
+      // bring its Q tile and first K, V tiles into L2 now.
+      if constexpr (MODE == 0) {
+        const int nxt = (int)blockIdx.x + p.prefetch_ahead;
+        if (ok && p.prefetch_ahead > 0 && nxt < (int)gridDim.x) {
+          const WideTile U = map_wide(p, nxt);
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_prefetch_l2_3d(&tm_q, c * 64, U.row0, U.bh);
+            if (U.n > 0) {
+              tma_prefetch_l2_3d(&tm_k, c * 64, U.krow0, U.bkv);
+              tma_prefetch_l2_3d(&tm_v, c * 64, U.krow0, U.bkv);
+            }
+          }
+        }
+      }
       if (!ok) {
         // Let the copies still in flight land before the CTA's shared memory goes away.
         const unsigned long long t0 = globaltimer_ns();
