@@ -293,12 +293,17 @@ template <int OFF>
 __device__ __forceinline__ void red_add_f32_at(float* base, float x) {
   asm volatile("red.global.add.f32 [%0+%1], %2;" ::"l"(base), "n"(OFF), "f"(x) : "memory");
 }
-// Pause after each 16 reductions of the drain (ns).  The drain has slack; spread out, its
-// reductions leave room in the load/store path for the compute warps' shared-memory
-// traffic.  Measured on GB300 (d = 128): 0 -> 100 ns gives +1 to +4 % across the
-// training, long, causal and deterministic shapes; 200 ns costs d = 64 and
-// deterministic runs 3 %.
-constexpr unsigned kDrainPauseNs = 100;
+// Pause after each 16 reductions of the drain (ns), per kernel instantiation.  The drain has
+// slack; spread out, its reductions leave room in the load/store path for the compute warps'
+// shared-memory traffic.  Measured on GB300: 0 -> 100 ns gave +1 to +4 % across the
+// training, long, causal and deterministic shapes at d = 128; with the L2 prefetch of the
+// next wave in place, 150 ns against 100 gives the atomic d = 128 kernel a further 1.4 to
+// 1.7 % (B4 H16 N2048, N = 8192 both masks) but costs d = 64 14 % and the deterministic
+// kernel 8 %, whose additions wait for their turn and do best with 50 ns (-0.9 %).
+template <int D, bool DET>
+__host__ __device__ constexpr unsigned drain_pause_ns() {
+  return DET ? 50u : (D == 128 ? 150u : 100u);
+}
 // Rows J0 .. J0 + 15 of a tile (row stride D floats), column = this lane.
 template <int D, int J0, int... J>
 __device__ __forceinline__ void red_add_chunk(float* base, const float (&v)[128], std::integer_sequence<int, J...>) {
@@ -306,10 +311,10 @@ __device__ __forceinline__ void red_add_chunk(float* base, const float (&v)[128]
 }
 // All 128 rows in chunks of 16, with a pause after each chunk so that the reductions
 // do not hold the load/store path while the compute warps need it.
-template <int D, int... C>
+template <int D, unsigned PAUSE, int... C>
 __device__ __forceinline__ void red_add_rows(float* base, const float (&v)[128], std::integer_sequence<int, C...>) {
   ((red_add_chunk<D, C * 16>(base, v, std::make_integer_sequence<int, 16>{}),
-    __nanosleep(kDrainPauseNs)), ...);
+    __nanosleep(PAUSE)), ...);
 }
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -893,7 +898,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       size_t arow;
       if constexpr (VL) arow = (size_t)bh * a.rows_pad + q0 + 128 * (size_t)b + (size_t)m * 128;
       else arow = (size_t)bh * a.nq * 128 + (size_t)m * 128;
-      red_add_rows<D>(acc + arow * D + dcol, v, std::make_integer_sequence<int, 8>{});
+      red_add_rows<D, drain_pause_ns<D, DET>()>(acc + arow * D + dcol, v, std::make_integer_sequence<int, 8>{});
     };
     if constexpr (!DET) {
       for (int it = 0; it < n_iter; ++it) {
