@@ -114,15 +114,17 @@ __device__ __forceinline__ void w_red_at(float* base, float x) {
   asm volatile("red.global.add.f32 [%0+%1], %2;" ::"l"(base), "n"(OFF), "f"(x) : "memory");
 }
 // Rows J0 .. J0 + 15 of a 64-row tile (row stride D floats), column = this lane, then a
-// short pause so that the reductions leave the load/store path to the compute warps.
-template <int D, int J0, int... J>
+// short pause so that the reductions leave the load/store path to the compute warps:
+// 150 ns with atomic dQ (measured on GB300 against 100 ns: 64-row tiles at d = 128 -2 %,
+// d = 256 -0.3 %, d = 192 unchanged), 100 ns when deterministic.
+template <int D, unsigned PAUSE, int J0, int... J>
 __device__ __forceinline__ void w_red_chunk(float* base, const float (&v)[64], std::integer_sequence<int, J...>) {
   (w_red_at<(J0 + J) * D * 4>(base, v[J0 + J]), ...);
-  __nanosleep(100);
+  __nanosleep(PAUSE);
 }
-template <int D, int... C>
+template <int D, unsigned PAUSE, int... C>
 __device__ __forceinline__ void w_red_rows(float* base, const float (&v)[64], std::integer_sequence<int, C...>) {
-  (w_red_chunk<D, C * 16>(base, v, std::make_integer_sequence<int, 16>{}), ...);
+  (w_red_chunk<D, PAUSE, C * 16>(base, v, std::make_integer_sequence<int, 16>{}), ...);
 }
 
 __device__ __forceinline__ int w_ld_acquire(const int* p) {
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     auto add_dq = [&](int bh, int m, const float (&v)[64]) {
       if (!has_col) return;
       const size_t arow = (size_t)bh * a.nq64 * 64 + (size_t)m * 64;
-      w_red_rows<D>(a.dq_acc + arow * D + c0 + dcol, v, std::make_integer_sequence<int, 4>{});
+      w_red_rows<D, (DET ? 100u : 150u)>(a.dq_acc + arow * D + c0 + dcol, v, std::make_integer_sequence<int, 4>{});
     };
     if constexpr (!DET) {
       for (int it = 0; it < n_iter; ++it) {
